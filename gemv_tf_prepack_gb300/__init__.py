@@ -1,0 +1,255 @@
+"""Python binding of libtf, the GB300 fused INT4/INT8-weight linear layer.
+
+Argument marshalling only: every step of the computation runs in libtf's
+CUDA kernels, reached through its C ABI (``include/tf.h``) with ctypes.
+PyTorch supplies device memory and streams.  There is no fallback: if
+``libtf.so`` has not been built, importing the device calls raises.
+
+    from gemv_tf_prepack_gb300 import prepack, Weights, gemv, gemm
+    blob = prepack(qweight, scales, zeros, N, K, bits=4, group=128)   # host, offline
+    W = Weights.upload(blob)                                          # device copy
+    y = gemv(W, x)     # x: torch.bfloat16 [M<=8, K] on the GPU -> y [M, N]
+    y = gemm(W, x)     # any M
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+__all__ = [
+    "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "unprepack",
+    "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemm", "device_error",
+    "header_declarations",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+lib_path = os.path.join(_HERE, "libtf.so")
+HEADER = os.path.join(_ROOT, "include", "tf.h")
+
+TF_OK = 0
+
+
+class TFError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        msg = _lib().tf_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{call}: {msg} ({status})")
+
+
+_LIB = None
+
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_p = ctypes.c_void_p
+
+_SIGNATURES = {
+    "tf_version": (_i, []),
+    "tf_status_string": (ctypes.c_char_p, [_i]),
+    "tf_prepack_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "tf_prepack": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _sz]),
+    "tf_unprepack": (_i, [_p, _sz, _p, _p, _p]),
+    "tf_blob_info": (_i, [_p, _sz] + [ctypes.POINTER(_i)] * 4),
+    "tf_dequant": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p]),
+    "tf_gemv_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "tf_gemv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
+    "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
+    "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
+}
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(lib_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def lib():
+    """The loaded ctypes library (loads it on first use)."""
+    return _lib()
+
+
+def _check(status: int, call: str):
+    if status != TF_OK:
+        raise TFError(status, call)
+
+
+def header_declarations():
+    """Names of the functions declared in include/tf.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(tf_\w+)\s*\(", text, re.M)))
+
+
+def version() -> int:
+    return _lib().tf_version()
+
+
+# ---------------------------------------------------------------------------
+# host: pre-tiling
+
+
+def prepack_size(N: int, K: int, bits: int, group: int) -> int:
+    out = _sz()
+    _check(_lib().tf_prepack_size(N, K, bits, group, ctypes.byref(out)), "tf_prepack_size")
+    return out.value
+
+
+def prepack(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, N: int, K: int,
+            bits: int, group: int) -> np.ndarray:
+    """Offline interleaved pre-tiling of natural-order inputs; returns the blob (uint8)."""
+    qw = np.ascontiguousarray(qweight, dtype=np.uint32 if bits == 4 else np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    z = np.ascontiguousarray(zeros, dtype=np.uint8)
+    g = K if group == 0 else group
+    want_qw = (N, K // 8) if bits == 4 else (N, K)
+    if qw.shape != want_qw or s.shape != (N, K // g) or z.shape != (N, K // g):
+        raise ValueError("qweight/scales/zeros shapes do not match N, K, bits, group")
+    out = np.empty(prepack_size(N, K, bits, group), dtype=np.uint8)
+    _check(_lib().tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, N, K, bits, group,
+                             out.ctypes.data, out.size), "tf_prepack")
+    return out
+
+
+def blob_info(blob: np.ndarray):
+    b = np.ascontiguousarray(blob, dtype=np.uint8)
+    v = [_i() for _ in range(4)]
+    _check(_lib().tf_blob_info(b.ctypes.data, b.size, *[ctypes.byref(x) for x in v]), "tf_blob_info")
+    return tuple(x.value for x in v)
+
+
+def unprepack(blob: np.ndarray):
+    """Exact inverse of prepack: (qweight, scales, zeros, N, K, bits, group)."""
+    b = np.ascontiguousarray(blob, dtype=np.uint8)
+    N, K, bits, group = blob_info(b)
+    g = K if group == 0 else group
+    qw = np.zeros((N, K // 8), np.uint32) if bits == 4 else np.zeros((N, K), np.uint8)
+    s = np.zeros((N, K // g), np.uint16)
+    z = np.zeros((N, K // g), np.uint8)
+    _check(_lib().tf_unprepack(b.ctypes.data, b.size, qw.ctypes.data, s.ctypes.data, z.ctypes.data),
+           "tf_unprepack")
+    return qw, s, z, N, K, bits, group
+
+
+# ---------------------------------------------------------------------------
+# device
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Weights:
+    """A device-resident blob plus its layer description."""
+
+    def __init__(self, blob_dev, N: int, K: int, bits: int, group: int):
+        self.blob = blob_dev
+        self.N, self.K, self.bits, self.group = N, K, bits, group
+        self._ws = {}
+
+    @classmethod
+    def upload(cls, blob: np.ndarray, device=None) -> "Weights":
+        torch = _torch()
+        N, K, bits, group = blob_info(blob)
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        t = torch.from_numpy(np.ascontiguousarray(blob, dtype=np.uint8)).to(dev)
+        return cls(t, N, K, bits, group)
+
+    @property
+    def nbytes(self) -> int:
+        return self.blob.numel()
+
+    def workspace(self, M: int):
+        """A zero-filled GEMV workspace for this layer and M (cached)."""
+        torch = _torch()
+        key = (M, self.blob.device)
+        if key not in self._ws:
+            n = gemv_workspace_size(self.N, self.K, self.bits, self.group, M)
+            self._ws[key] = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.blob.device)
+        return self._ws[key]
+
+
+def gemv_workspace_size(N: int, K: int, bits: int, group: int, M: int) -> int:
+    out = _sz()
+    _check(_lib().tf_gemv_workspace_size(N, K, bits, group, M, ctypes.byref(out)),
+           "tf_gemv_workspace_size")
+    return out.value
+
+
+def _check_x(W: Weights, x):
+    torch = _torch()
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != W.K or not x.is_cuda:
+        raise ValueError(f"x must be a CUDA bfloat16 tensor [M, {W.K}]")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+
+
+def _out(W: Weights, M: int, y):
+    torch = _torch()
+    if y is None:
+        return torch.empty((M, W.N), dtype=torch.bfloat16, device=W.blob.device)
+    if y.dtype != torch.bfloat16 or tuple(y.shape) != (M, W.N) or not y.is_contiguous():
+        raise ValueError(f"y must be a contiguous bfloat16 tensor [{M}, {W.N}]")
+    return y
+
+
+def dequant(W: Weights, out=None, stream=None):
+    """Dense BF16 W [N, K] from the blob, with the kernels' exact dequant arithmetic."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((W.N, W.K), dtype=torch.bfloat16, device=W.blob.device)
+    _check(_lib().tf_dequant(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(out),
+                             _stream(stream)), "tf_dequant")
+    return out
+
+
+def gemv(W: Weights, x, y=None, workspace=None, stream=None):
+    """y[M, N] = x[M, K] W^T for 1 <= M <= 8 (fused unpack + dequant + mma.sync, split-K)."""
+    _check_x(W, x)
+    M = x.shape[0]
+    y = _out(W, M, y)
+    ws = W.workspace(M) if workspace is None else workspace
+    _check(_lib().tf_gemv(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
+                          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "tf_gemv")
+    return y
+
+
+def gemm(W: Weights, x, y=None, stream=None):
+    """y[M, N] = x[M, K] W^T for any M (fused dequant to SMEM + tcgen05 MMAs)."""
+    _check_x(W, x)
+    M = x.shape[0]
+    y = _out(W, M, y)
+    _check(_lib().tf_gemm(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
+                          _stream(stream)), "tf_gemm")
+    return y
+
+
+def device_error() -> int:
+    """Read and clear the current device's error word (synchronous)."""
+    v = ctypes.c_uint()
+    _check(_lib().tf_device_error(ctypes.byref(v)), "tf_device_error")
+    return v.value

@@ -1,0 +1,413 @@
+// Fused prefill GEMM of libtf on the 5th-generation tensor cores.
+//
+// TileFuse, Methodology 1: each weight tile is unpacked and dequantised
+// *once* into on-chip memory and the BF16 result is reused for the tile's
+// matrix operations.  Here, per CTA output tile of 128 weight rows x BN
+// tokens (BN <= 256):
+//   warp 0       streams pre-tiled weight tiles (one 1-D bulk copy each: a
+//                tile is contiguous and carries its own scales and zeros)
+//                and the matching activation slabs (2-D TMA, 128-byte
+//                swizzle) into shared-memory rings;
+//   warps 6..13  unpack + dequantise one 16-row block each into the UMMA
+//                K-major 128-byte-swizzled layout (bit-exact
+//                bf16_rne((q - z) * s)), 64 K-columns at a time;
+//   warp 1       issues tcgen05.mma (M = 128 weight rows, N = BN tokens,
+//                K = 16) from one thread, accumulating in tensor memory;
+//                two accumulators let the epilogue of one tile overlap the
+//                MMAs of the next;
+//   warps 2..5   read the accumulator with tcgen05.ld, round to BF16 and
+//                store y.
+// Each dequantised 128 x 64 weight slab feeds BN/16 * 4 MMAs, i.e. it is
+// reused across all BN tokens of the tile.  CTAs are persistent (one per
+// SM) and walk output tiles with the token index fastest, so CTAs that run
+// together share weight tiles in L2.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/tf.h"
+#include "tf_abi.h"
+#include "tf_device.cuh"
+#include "tf_format.h"
+#include "tf_sm100.cuh"
+
+namespace tf {
+
+// Device-side error word (first error wins); read by tf_device_error.
+__device__ unsigned g_tf_error;
+
+namespace {
+
+constexpr int kThreads = 448;        // 14 warps
+constexpr int kDequantWarp0 = 6;     // warps 6..13
+constexpr int kEpilogueWarp0 = 2;    // warps 2..5
+constexpr int kSlabBytesW = 128 * 128;  // 128 rows x 64 BF16
+constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+
+enum : unsigned {
+  kErrProducerWait = 0x100,
+  kErrDequantWait = 0x200,
+  kErrMmaWait = 0x300,
+  kErrEpilogueWait = 0x400,
+  kErrDrain = 0x500,
+};
+
+struct GemmArgs {
+  const uint8_t* tiles;
+  uint16_t* y;
+  int N, K, M, KT, g, tile_bytes;
+  int MT, BN, ntiles;
+  int P, OPS;                 // stages of the packed ring and of the operand ring
+  int off_op, off_bar;        // byte offsets in the 1024-aligned dynamic smem
+};
+
+struct Bars {
+  uint32_t full_p, empty_p, full_op, empty_op, tfull, tempty, drain, tmem_slot;
+};
+
+__device__ __forceinline__ Bars bars_at(uint32_t base, int P, int OPS) {
+  Bars b;
+  b.full_p = base;
+  b.empty_p = b.full_p + 8 * P;
+  b.full_op = b.empty_p + 8 * P;
+  b.empty_op = b.full_op + 8 * OPS;
+  b.tfull = b.empty_op + 8 * OPS;
+  b.tempty = b.tfull + 16;
+  b.drain = b.tempty + 16;
+  b.tmem_slot = b.drain + 8;
+  return b;
+}
+
+template <int BITS, int GPT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                           const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Bars B = bars_at(sbase + a.off_bar, a.P, a.OPS);
+  const uint32_t x_slab_bytes = (uint32_t)a.BN * 128;
+  const uint32_t op_stage_bytes = kSlabBytesW + x_slab_bytes;
+  unsigned* err = &g_tf_error;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.P; ++i) {
+      mbar_init(B.full_p + 8 * i, 1);
+      mbar_init(B.empty_p + 8 * i, 8);
+    }
+    for (int i = 0; i < a.OPS; ++i) {
+      mbar_init(B.full_op + 8 * i, 1 + 8);  // producer (with tx) + 8 dequant warps
+      mbar_init(B.empty_op + 8 * i, 1);     // tcgen05.commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B.tfull + 8 * i, 1);
+      mbar_init(B.tempty + 8 * i, 4);
+    }
+    mbar_init(B.drain, 1);
+    mbar_init_fence();
+    prefetch_tensormap(&tmx);
+  }
+  if (warp == 1) {
+    tmem_alloc(B.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + (B.tmem_slot - sbase));
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int ps = 0, os = 0;
+      uint32_t pph = 0, oph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+        const int nb = tile / a.MT, mt = tile - nb * a.MT;
+        const uint8_t* src = a.tiles + (size_t)nb * a.KT * a.tile_bytes;
+        for (int kt = 0; kt < a.KT && ok; ++kt) {
+          ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
+          if (!ok) break;
+          mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
+          bulk_load(sbase + (uint32_t)ps * a.tile_bytes, src + (size_t)kt * a.tile_bytes, (uint32_t)a.tile_bytes,
+                    B.full_p + 8 * ps);
+          if (++ps == a.P) { ps = 0; pph ^= 1; }
+          for (int h = 0; h < 2; ++h) {
+            ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
+            if (!ok) break;
+            mbar_arrive_expect_tx(B.full_op + 8 * os, x_slab_bytes);
+            tma_load_2d(sbase + a.off_op + (uint32_t)os * op_stage_bytes + kSlabBytesW, &tmx,
+                        kt * kTileK + h * 64, mt * a.BN, B.full_op + 8 * os);
+            if (++os == a.OPS) { os = 0; oph ^= 1; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, a.BN);
+      int os = 0, acc = 0;
+      uint32_t oph = 0, aph = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+        ok = mbar_wait(B.tempty + 8 * acc, aph ^ 1, err, kErrMmaWait, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * 256;
+        const int nslabs = 2 * a.KT;
+        for (int sl = 0; sl < nslabs; ++sl) {
+          ok = mbar_wait(B.full_op + 8 * os, oph, err, kErrMmaWait, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t wsl = sbase + a.off_op + (uint32_t)os * op_stage_bytes;
+          const uint64_t ad = smem_desc_kmajor_sw128(wsl);
+          const uint64_t bd = smem_desc_kmajor_sw128(wsl + kSlabBytesW);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes inside the swizzle atom
+            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (sl | kk) ? 1u : 0u);
+          umma_commit(B.empty_op + 8 * os);
+          issued = true;
+          if (++os == a.OPS) { os = 0; oph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(B.tfull + 8 * acc);
+        if (++acc == 2) { acc = 0; aph ^= 1; }
+      }
+      if (issued) {
+        // wait for every MMA of this CTA before tensor memory is released
+        umma_commit(B.drain);
+        mbar_wait(B.drain, 0, err, kErrDrain, kTimeoutNs);
+      }
+    }
+  } else if (warp >= kEpilogueWarp0 && warp < kDequantWarp0) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+      const int nb = tile / a.MT, mt = tile - nb * a.MT;
+      ok = mbar_wait(B.tfull + 8 * acc, aph, err, kErrEpilogueWait, kTimeoutNs);
+      if (!ok) break;
+      tc_fence_after();
+      const int n = nb * kTileN + q * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256;
+      for (int c0 = 0; c0 < a.BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_16(taddr + (uint32_t)c0, r);
+        tmem_ld_wait();
+        const int m0 = mt * a.BN + c0;
+        if (n < a.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + j;
+            if (m < a.M)
+              a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.tempty + 8 * acc);
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+  } else {
+    // ---------------------------------------------------------------- dequant
+    const int mb = warp - kDequantWarp0;  // 16-row block of every tile
+    const int gr = lane & 7, t = lane >> 3;  // lane reads slot p = lane (conflict-free)
+    constexpr int WB = kTileN * kTileK * BITS / 8;
+    constexpr int SB = BITS == 4 ? 16 : 32;
+    constexpr int ZB = BITS == 4 ? 64 : 128;
+    const int r0 = mb * 16 + gr;  // rows r0 and r0 + 8 of the 128-row slab
+    // byte offsets of this lane's two 16-byte chunks in rows r0, r0 + 8
+    uint32_t dst[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = r0 + 8 * e;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int chunk = 2 * t + cc;
+        dst[e][cc] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
+      }
+    }
+    int ps = 0, os = 0;
+    uint32_t pph = 0, oph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+      for (int kt = 0; kt < a.KT && ok; ++kt) {
+        ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, kTimeoutNs);
+        if (!ok) break;
+        const uint8_t* pk = smem + (size_t)ps * a.tile_bytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int gi = GPT == 1 ? 0 : (h * 64 + 16 * t) / a.g;
+          const uint32_t sp = *reinterpret_cast<const uint32_t*>(pk + WB + gi * 256 + (mb * 8 + gr) * 4);
+          const uint8_t* slot = pk + ((mb * 2 + h) * 32 + lane) * SB;
+          uint32_t lo[8], hi[8];
+          if (BITS == 4) {
+            const MetaW4 m = meta_w4(sp, pk[WB + GPT * 256 + gi * ZB + mb * 8 + gr]);
+            const uint4 v = *reinterpret_cast<const uint4*>(slot);
+            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t f[4];
+              dequant_w4(words[j], m, f);
+              lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
+              hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
+            }
+          } else {
+            const uint32_t zp = *reinterpret_cast<const uint16_t*>(pk + WB + GPT * 256 + gi * ZB + (mb * 8 + gr) * 2);
+            const MetaW8 m = meta_w8(sp, zp);
+            const uint4 v0 = reinterpret_cast<const uint4*>(slot)[0];
+            const uint4 v1 = reinterpret_cast<const uint4*>(slot)[1];
+            const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t f[4];
+              dequant_w8(words[2 * j], words[2 * j + 1], m, f);
+              lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
+              hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
+            }
+          }
+          ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, kTimeoutNs);
+          if (!ok) break;
+          uint8_t* wsl = smem + a.off_op + (size_t)os * op_stage_bytes;
+          *reinterpret_cast<uint4*>(wsl + dst[0][0]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(wsl + dst[0][1]) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+          *reinterpret_cast<uint4*>(wsl + dst[1][0]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(wsl + dst[1][1]) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.full_op + 8 * os);
+          if (++os == a.OPS) { os = 0; oph ^= 1; }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.empty_p + 8 * ps);
+        if (++ps == a.P) { ps = 0; pph ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxSmem = 227 * 1024;
+
+struct GemmPlan {
+  GemmArgs a;
+  size_t smem;
+  int grid;
+};
+
+int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
+  GemmArgs& a = P->a;
+  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
+  a.BN = M >= 256 ? 256 : (M + 15) / 16 * 16;
+  a.MT = (M + a.BN - 1) / a.BN;
+  a.ntiles = G.NB * a.MT;
+  const int op_stage = kSlabBytesW + a.BN * 128;
+  a.OPS = 0;
+  for (int ops = 4; ops >= 2 && a.OPS == 0; --ops)
+    for (int p = 4; p >= 2; --p) {
+      const int off_op = (p * G.tile_bytes + 1023) / 1024 * 1024;
+      const int off_bar = off_op + ops * op_stage;
+      const size_t smem = 1024 + off_bar + 256;
+      if (smem <= (size_t)kMaxSmem) {
+        a.P = p; a.OPS = ops; a.off_op = off_op; a.off_bar = off_bar;
+        P->smem = smem;
+        break;
+      }
+    }
+  if (a.OPS == 0) return TF_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return TF_ERR_CUDA;
+  P->grid = a.ntiles < sms ? a.ntiles : sms;
+  return TF_OK;
+}
+
+template <int BITS, int GPT>
+int launch_gemm(const CUtensorMap& map, const GemmPlan& P, cudaStream_t s) {
+  auto kfn = gemm_kernel<BITS, GPT>;
+  // The attribute is per function; setting it is cheap and thread-safe.
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem) != cudaSuccess)
+    return TF_ERR_CUDA;
+  kfn<<<P.grid, kThreads, P.smem, s>>>(map, P.a);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace tf
+
+using namespace tf;
+
+extern "C" {
+
+int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x, uint16_t* y,
+            int M, cudaStream_t stream) {
+  Geometry G;
+  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
+  if (rc) return rc;
+  if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return TF_ERR_ALIGNMENT;
+  GemmPlan P;
+  rc = gemm_plan(G, M, &P);
+  if (rc) return rc;
+  P.a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  P.a.y = y;
+  auto enc = encode_fn();
+  if (!enc) return TF_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)P.a.BN};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return TF_ERR_CUDA;
+  if (bits == 4) {
+    if (G.gpt == 1) return launch_gemm<4, 1>(map, P, stream);
+    if (G.gpt == 2) return launch_gemm<4, 2>(map, P, stream);
+    return launch_gemm<4, 4>(map, P, stream);
+  }
+  if (G.gpt == 1) return launch_gemm<8, 1>(map, P, stream);
+  if (G.gpt == 2) return launch_gemm<8, 2>(map, P, stream);
+  return launch_gemm<8, 4>(map, P, stream);
+}
+
+int tf_device_error(unsigned int* code) {
+  if (!code) return TF_ERR_INVALID_ARG;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tf_error, sizeof v) != cudaSuccess) return TF_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_tf_error, &zero, sizeof zero) != cudaSuccess) return TF_ERR_CUDA;
+  *code = v;
+  return TF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,261 @@
+// Host side of libtf: the offline interleaved pre-tiling (TileFuse,
+// Methodology 2 "Interleaved pre-tiling": quantisation metadata packed into
+// the weight tiles, matrix reordered so that each consumer's tiles are
+// contiguous, valid up to 32K), its exact inverse, and the small status API.
+#include <algorithm>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "../../include/tf.h"
+#include "tf_format.h"
+
+using tf::Geometry;
+
+namespace {
+
+// Natural-order accessors with the padding rules of the blob format.
+struct Source {
+  const Geometry& G;
+  const uint8_t* q8;     // INT8 codes [N, K]
+  const uint32_t* q4;    // INT4 words [N, K/8]
+  const uint16_t* s;     // [N, K/g]
+  const uint8_t* z;      // [N, K/g]
+  int n_groups;
+
+  int code(int n, int k) const {
+    if (G.bits == 4) return (q4[(size_t)n * (G.K / 8) + (k >> 3)] >> (4 * (k & 7))) & 0xF;
+    return q8[(size_t)n * G.K + k];
+  }
+  // Group of padded column k (k may lie in the K padding of the last tile).
+  int group_of(int k) const {
+    return G.gpt > 1 ? k / G.g : (k / tf::kTileK * tf::kTileK) / G.g;
+  }
+  int padded_code(int n, int k) const {
+    if (n >= G.N) return 0;
+    if (k < G.K) return code(n, k);
+    const int grp = group_of(k);
+    return grp < n_groups ? z[(size_t)n * n_groups + grp] : 0;
+  }
+  uint16_t scale(int n, int grp) const {
+    return (n < G.N && grp < n_groups) ? s[(size_t)n * n_groups + grp] : 0;
+  }
+  uint8_t zero(int n, int grp) const {
+    return (n < G.N && grp < n_groups) ? z[(size_t)n * n_groups + grp] : 0;
+  }
+};
+
+// Tile row / column of code i of word j in slot p of block (mb, h).
+inline void code_position(int mb, int h, int p, int j, int i, int* row, int* col) {
+  const int gr = p & 7, t = p >> 3, r = i & 3, e = i >> 2;
+  *row = mb * 16 + gr + 8 * (r & 1);
+  *col = h * 64 + 16 * t + 4 * j + 2 * (r >> 1) + e;
+}
+
+void pack_tile(const Source& src, int nb, int kt, uint8_t* tile) {
+  const Geometry& G = src.G;
+  const int sb = tf::slot_bytes(G.bits);
+  for (int mb = 0; mb < 8; ++mb)
+    for (int h = 0; h < 2; ++h)
+      for (int p = 0; p < 32; ++p) {
+        uint8_t* slot = tile + ((mb * 2 + h) * 32 + p) * sb;
+        for (int j = 0; j < 4; ++j) {
+          uint32_t word = 0;
+          for (int i = 0; i < 8; ++i) {
+            int row, col;
+            code_position(mb, h, p, j, i, &row, &col);
+            const int c = src.padded_code(nb * tf::kTileN + row, kt * tf::kTileK + col);
+            if (G.bits == 4)
+              word |= (uint32_t)c << (4 * i);
+            else
+              slot[8 * j + i] = (uint8_t)c;
+          }
+          if (G.bits == 4) {
+            for (int b = 0; b < 4; ++b) slot[4 * j + b] = (uint8_t)(word >> (8 * b));
+          }
+        }
+      }
+  uint8_t* sptr = tile + tf::tile_weight_bytes(G.bits);
+  uint8_t* zptr = sptr + 256 * G.gpt;
+  const int zb = tf::tile_zero_bytes(G.bits);
+  for (int gi = 0; gi < G.gpt; ++gi) {
+    const int grp = src.group_of(kt * tf::kTileK + (G.gpt > 1 ? gi * G.g : 0));
+    for (int mb = 0; mb < 8; ++mb)
+      for (int gr = 0; gr < 8; ++gr)
+        for (int e = 0; e < 2; ++e) {
+          const int n = nb * tf::kTileN + mb * 16 + gr + 8 * e;
+          const uint16_t s = src.scale(n, grp);
+          uint8_t* d = sptr + gi * 256 + ((mb * 8 + gr) * 2 + e) * 2;
+          d[0] = (uint8_t)(s & 0xFF);
+          d[1] = (uint8_t)(s >> 8);
+          const uint8_t z = src.zero(n, grp);
+          if (G.bits == 4) {
+            uint8_t& zz = zptr[gi * zb + mb * 8 + gr];
+            if (e == 0) zz = (uint8_t)((zz & 0xF0) | z);
+            else zz = (uint8_t)((zz & 0x0F) | (z << 4));
+          } else {
+            zptr[gi * zb + (mb * 8 + gr) * 2 + e] = z;
+          }
+        }
+  }
+}
+
+void write_header(const Geometry& G, uint8_t* out) {
+  tf::BlobHeader h;
+  std::memset(&h, 0, sizeof h);
+  h.magic = tf::kMagic;
+  h.version = tf::kVersion;
+  h.N = G.N; h.K = G.K; h.bits = G.bits; h.group = G.group;
+  h.tile_n = tf::kTileN; h.tile_k = tf::kTileK;
+  h.NB = G.NB; h.KT = G.KT; h.tile_bytes = G.tile_bytes; h.groups_per_tile = G.gpt;
+  h.total_bytes = G.total_bytes;
+  std::memcpy(out, &h, sizeof h);  // the ABI is little-endian
+}
+
+template <class F>
+void parallel_rows(int NB, F&& f) {
+  unsigned nt = std::max(1u, std::min(std::thread::hardware_concurrency(), 32u));
+  nt = std::min<unsigned>(nt, (unsigned)NB);
+  if (nt <= 1) {
+    for (int nb = 0; nb < NB; ++nb) f(nb);
+    return;
+  }
+  std::vector<std::thread> th;
+  for (unsigned w = 0; w < nt; ++w)
+    th.emplace_back([&, w] {
+      for (int nb = (int)w; nb < NB; nb += (int)nt) f(nb);
+    });
+  for (auto& t : th) t.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+int tf_version(void) { return TF_VERSION; }
+
+const char* tf_status_string(int status) {
+  switch (status) {
+    case TF_OK: return "TF_OK";
+    case TF_ERR_INVALID_ARG: return "TF_ERR_INVALID_ARG: null pointer, bad size or bad combination";
+    case TF_ERR_UNSUPPORTED: return "TF_ERR_UNSUPPORTED: dimension, bits/group or M not supported";
+    case TF_ERR_ALIGNMENT: return "TF_ERR_ALIGNMENT: device pointer not 16-byte aligned";
+    case TF_ERR_WORKSPACE: return "TF_ERR_WORKSPACE: workspace missing or too small";
+    case TF_ERR_BAD_BLOB: return "TF_ERR_BAD_BLOB: blob header or size mismatch";
+    case TF_ERR_CUDA: return "TF_ERR_CUDA: CUDA runtime call or launch failed";
+    case TF_ERR_DEVICE: return "TF_ERR_DEVICE: a kernel reported an error";
+    default: return "unknown tf status";
+  }
+}
+
+int tf_prepack_size(int N, int K, int bits, int group, size_t* bytes) {
+  if (!bytes) return TF_ERR_INVALID_ARG;
+  Geometry G;
+  int rc = tf::make_geometry(N, K, bits, group, &G);
+  if (rc) return rc;
+  *bytes = G.total_bytes;
+  return TF_OK;
+}
+
+int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros, int N, int K,
+               int bits, int group, void* out, size_t out_bytes) {
+  if (!qweight || !scales || !zeros || !out) return TF_ERR_INVALID_ARG;
+  Geometry G;
+  int rc = tf::make_geometry(N, K, bits, group, &G);
+  if (rc) return rc;
+  if (out_bytes < G.total_bytes) return TF_ERR_INVALID_ARG;
+  const int n_groups = K / G.g;
+  const int qmax = (1 << bits) - 1;
+  for (size_t i = 0; i < (size_t)N * n_groups; ++i)
+    if (zeros[i] > qmax) return TF_ERR_INVALID_ARG;
+  Source src{G, (const uint8_t*)qweight, (const uint32_t*)qweight, scales, zeros, n_groups};
+  uint8_t* o = (uint8_t*)out;
+  write_header(G, o);
+  parallel_rows(G.NB, [&](int nb) {
+    for (int kt = 0; kt < G.KT; ++kt) {
+      uint8_t* tile = o + tf::kHeaderBytes + ((size_t)nb * G.KT + kt) * G.tile_bytes;
+      std::memset(tile, 0, G.tile_bytes);
+      pack_tile(src, nb, kt, tile);
+    }
+  });
+  return TF_OK;
+}
+
+int tf_blob_info(const void* header, size_t bytes, int* N, int* K, int* bits, int* group) {
+  if (!header || bytes < (size_t)tf::kHeaderBytes) return TF_ERR_INVALID_ARG;
+  tf::BlobHeader h;
+  std::memcpy(&h, header, sizeof h);
+  if (h.magic != tf::kMagic || h.version != tf::kVersion) return TF_ERR_BAD_BLOB;
+  Geometry G;
+  if (tf::make_geometry(h.N, h.K, h.bits, h.group, &G)) return TF_ERR_BAD_BLOB;
+  if (h.tile_n != tf::kTileN || h.tile_k != tf::kTileK || h.NB != G.NB || h.KT != G.KT ||
+      h.tile_bytes != G.tile_bytes || h.groups_per_tile != G.gpt || h.total_bytes != G.total_bytes)
+    return TF_ERR_BAD_BLOB;
+  if (N) *N = h.N;
+  if (K) *K = h.K;
+  if (bits) *bits = h.bits;
+  if (group) *group = h.group;
+  return TF_OK;
+}
+
+int tf_unprepack(const void* blob, size_t bytes, void* qweight, uint16_t* scales, uint8_t* zeros) {
+  if (!blob || !qweight || !scales || !zeros) return TF_ERR_INVALID_ARG;
+  int N, K, bits, group;
+  int rc = tf_blob_info(blob, bytes, &N, &K, &bits, &group);
+  if (rc) return rc;
+  Geometry G;
+  tf::make_geometry(N, K, bits, group, &G);
+  if (bytes < G.total_bytes) return TF_ERR_BAD_BLOB;
+  const uint8_t* b = (const uint8_t*)blob;
+  const int n_groups = K / G.g;
+  const int sb = tf::slot_bytes(bits);
+  const int zb = tf::tile_zero_bytes(bits);
+  if (bits == 4) std::memset(qweight, 0, (size_t)N * (K / 8) * 4);
+  parallel_rows(G.NB, [&](int nb) {
+    for (int kt = 0; kt < G.KT; ++kt) {
+      const uint8_t* tile = b + tf::kHeaderBytes + ((size_t)nb * G.KT + kt) * G.tile_bytes;
+      for (int mb = 0; mb < 8; ++mb)
+        for (int h = 0; h < 2; ++h)
+          for (int p = 0; p < 32; ++p) {
+            const uint8_t* slot = tile + ((mb * 2 + h) * 32 + p) * sb;
+            for (int j = 0; j < 4; ++j)
+              for (int i = 0; i < 8; ++i) {
+                int row, col;
+                code_position(mb, h, p, j, i, &row, &col);
+                const int n = nb * tf::kTileN + row, k = kt * tf::kTileK + col;
+                if (n >= N || k >= K) continue;
+                int c;
+                if (bits == 4) {
+                  const uint32_t w = (uint32_t)slot[4 * j] | ((uint32_t)slot[4 * j + 1] << 8) |
+                                     ((uint32_t)slot[4 * j + 2] << 16) | ((uint32_t)slot[4 * j + 3] << 24);
+                  c = (w >> (4 * i)) & 0xF;
+                  ((uint32_t*)qweight)[(size_t)n * (K / 8) + (k >> 3)] |= (uint32_t)c << (4 * (k & 7));
+                } else {
+                  ((uint8_t*)qweight)[(size_t)n * K + k] = slot[8 * j + i];
+                }
+              }
+          }
+      const uint8_t* sptr = tile + tf::tile_weight_bytes(bits);
+      const uint8_t* zptr = sptr + 256 * G.gpt;
+      for (int gi = 0; gi < G.gpt; ++gi) {
+        const int c0 = kt * tf::kTileK + (G.gpt > 1 ? gi * G.g : 0);
+        if (c0 >= K) continue;
+        const int grp = c0 / G.g;
+        for (int mb = 0; mb < 8; ++mb)
+          for (int gr = 0; gr < 8; ++gr)
+            for (int e = 0; e < 2; ++e) {
+              const int n = nb * tf::kTileN + mb * 16 + gr + 8 * e;
+              if (n >= N) continue;
+              const uint8_t* d = sptr + gi * 256 + ((mb * 8 + gr) * 2 + e) * 2;
+              scales[(size_t)n * n_groups + grp] = (uint16_t)(d[0] | (d[1] << 8));
+              zeros[(size_t)n * n_groups + grp] =
+                  bits == 4 ? (uint8_t)((zptr[gi * zb + mb * 8 + gr] >> (4 * e)) & 0xF)
+                            : zptr[gi * zb + (mb * 8 + gr) * 2 + e];
+            }
+      }
+    }
+  });
+  return TF_OK;
+}
+
+}  // extern "C"

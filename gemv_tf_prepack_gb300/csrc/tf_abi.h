@@ -1,0 +1,51 @@
+// Argument checks and device queries shared by the ABI entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/tf.h"
+#include "tf_format.h"
+
+namespace tf {
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Streaming multiprocessors of the current device (cached per device).
+inline int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Common validation of a device blob against the layer description.
+inline int check_blob(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                      Geometry* G) {
+  int rc = make_geometry(N, K, bits, group, G);
+  if (rc) return rc;
+  if (!blob) return TF_ERR_INVALID_ARG;
+  if (!aligned16(blob)) return TF_ERR_ALIGNMENT;
+  if (blob_bytes != G->total_bytes) return TF_ERR_BAD_BLOB;
+  return TF_OK;
+}
+
+// Status of the launch just made; peeks so that unrelated sticky errors of
+// other libraries are neither reported as ours nor cleared.
+inline int launch_status() {
+  cudaError_t e = cudaPeekAtLastError();
+  if (e == cudaSuccess) return TF_OK;
+  cudaGetLastError();  // a launch error of ours is not sticky; clear it
+  return TF_ERR_CUDA;
+}
+
+}  // namespace tf

@@ -1,0 +1,158 @@
+/*
+ * tf.h — C ABI of libtf: a GB300 (sm_103a) fused mixed-precision linear layer.
+ *
+ * The operation is the one the TileFuse pages describe ("TileFuse: A Fused
+ * Mixed-Precision Kernel Library for Efficient Quantized LLM Inference on
+ * AMD NPUs", section "Methodology", item 1 "Fused mixed-precision
+ * microkernels"): AWQ-style packed INT4/INT8 weights are unpacked,
+ * dequantised per group or per channel to BF16 as (q - zero) * scale, and
+ * consumed in the same kernel by a GEMV (token generation, batch 1) or a
+ * GEMM (prefill):
+ *
+ *     y[m, n] = sum_k x[m, k] * bf16_rne((q[n, k] - z[n, k/g]) * s[n, k/g])
+ *
+ * with x BF16 [M, K], y BF16 [M, N], FP32 accumulation and one final
+ * round-to-nearest-even to BF16.  W is N (out) x K (in).
+ *
+ * Conventions shared by every call:
+ *  - bits is 4 or 8.  group is 32, 64, any multiple of 128 that divides K,
+ *    or 0 for per output channel (one group spanning all of K).  K must be
+ *    a multiple of 8 and of the group.  1 <= N, K <= 32768 (the pages'
+ *    "dimensions up to 32K", Contributions 2).
+ *  - BF16 values are passed as their uint16 bit patterns.
+ *  - Natural-order inputs (host memory): INT4 qweight is uint32 [N, K/8],
+ *    eight codes per word, low nibble first along K; INT8 qweight is uint8
+ *    [N, K]; scales uint16 [N, K/g]; zeros uint8 [N, K/g] (0..2^bits-1).
+ *  - The caller allocates and owns every buffer.  The library allocates no
+ *    memory; its only global state is cached device attributes and one
+ *    device-side error word per device.
+ *  - Every call returns TF_OK (0) or a negative TF_ERR_* code and never
+ *    aborts.  Device calls only enqueue work on the given stream (NULL means
+ *    the legacy default stream) and return without synchronising; a
+ *    TF_ERR_CUDA return means the launch itself failed.
+ *  - Calls are thread-safe.  Two device calls that share a workspace must
+ *    not run concurrently.
+ */
+#ifndef TF_H_
+#define TF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TF_VERSION 1
+
+#define TF_OK 0
+#define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */
+#define TF_ERR_UNSUPPORTED (-2) /* dims > 32768, bits/group not supported, M too large for the call */
+#define TF_ERR_ALIGNMENT (-3)   /* a device pointer is not 16-byte aligned */
+#define TF_ERR_WORKSPACE (-4)   /* workspace missing or smaller than required */
+#define TF_ERR_BAD_BLOB (-5)    /* header magic/version/fields do not match */
+#define TF_ERR_CUDA (-6)        /* a CUDA runtime call or a launch failed */
+#define TF_ERR_DEVICE (-7)      /* a kernel reported an error (see tf_device_error) */
+
+/* Library version (TF_VERSION). */
+int tf_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* tf_status_string(int status);
+
+/*
+ * Pre-tiled blob format ("interleaved pre-tiling", Methodology 2: metadata is
+ * packed into the weight tiles and the matrix is reordered so that each
+ * consumer's tiles are contiguous, valid up to 32K).
+ *
+ * Blob = 64-byte header + NB*KT tiles (NB = ceil(N/128), KT = ceil(K/128)),
+ * tile (nb, kt) at byte 64 + (nb*KT + kt) * tile_bytes.  A tile holds a
+ * 128 x 128 block of codes in mma.sync fragment order, then its BF16 scales,
+ * then its zeros, so one contiguous read brings everything the tile needs.
+ * The header is little-endian: u32 magic 0x4B504654, u32 version 1, i32 N,
+ * K, bits, group, tile_n (128), tile_k (128), NB, KT, tile_bytes,
+ * groups_per_tile, u64 total_bytes, 8 zero bytes.  Padding rows (n >= N)
+ * and columns (k >= K) dequantise to exactly zero.
+ */
+
+/* Size in bytes of the blob for this layer; writes *bytes. */
+int tf_prepack_size(int N, int K, int bits, int group, size_t* bytes);
+
+/*
+ * Offline pre-tiling (host, synchronous, pure).  qweight / scales / zeros are
+ * host arrays in natural order (see above); out is a host buffer of at least
+ * tf_prepack_size bytes.  Codes or zeros above 2^bits - 1 give
+ * TF_ERR_INVALID_ARG.  The caller uploads the blob to the device.
+ */
+int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros,
+               int N, int K, int bits, int group, void* out, size_t out_bytes);
+
+/*
+ * Exact inverse of tf_prepack (host).  Reads N, K, bits, group from the
+ * header and writes natural-order qweight, scales and zeros (sizes as for
+ * tf_prepack).  TF_ERR_BAD_BLOB if the header is inconsistent with bytes.
+ */
+int tf_unprepack(const void* blob, size_t bytes, void* qweight, uint16_t* scales,
+                 uint8_t* zeros);
+
+/* Parse a host copy of the 64-byte header; any output pointer may be NULL. */
+int tf_blob_info(const void* header, size_t bytes, int* N, int* K, int* bits, int* group);
+
+/*
+ * Debug / parity path: dequantise the whole device-resident blob to dense
+ * BF16 w[N, K] (row-major, device memory) with exactly the unpack and
+ * dequant arithmetic the GEMV and GEMM kernels use
+ * (bf16_rne((q - z) * s), Methodology 1).  blob and w must be 16-byte
+ * aligned; blob_bytes is the blob's size (checked against N, K, bits, group).
+ */
+int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+               uint16_t* w, cudaStream_t stream);
+
+/*
+ * Workspace bytes tf_gemv needs on the current device for this layer and M
+ * (split-K partial sums plus per-block arrival counters).  The workspace must
+ * be zero-filled before its first use; every tf_gemv leaves it zero-filled
+ * again, so one workspace can be reused by calls ordered on one stream.
+ */
+int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
+
+/*
+ * Fused GEMV for token generation ("GEMV dataflow co-design", Methodology 3;
+ * batch 1, and up to 8 rows at no extra cost): y[M, N] = x[M, K] * W^T.
+ * Each weight code is read from HBM once, unpacked and dequantised to BF16 in
+ * registers and fed straight to the tensor cores (mma.sync, FP32
+ * accumulation).  The K dimension is split across all SMs so that the whole
+ * chip streams weights; partial sums are combined by the last-arriving block
+ * in a fixed order, so results are deterministic run to run.
+ * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),
+ * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size).
+ * 1 <= M <= 8, else TF_ERR_UNSUPPORTED.
+ */
+int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+            const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
+            cudaStream_t stream);
+
+/*
+ * Fused GEMM for prefill (Methodology 1: each weight tile is unpacked and
+ * dequantised once into on-chip memory and reused for the tile's MMAs):
+ * y[M, N] = x[M, K] * W^T for any M >= 1, with tcgen05 tensor-core MMAs
+ * accumulating in tensor memory.  Device pointers: blob, x and y 16-byte
+ * aligned.  No workspace.
+ */
+int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+            const uint16_t* x, uint16_t* y, int M, cudaStream_t stream);
+
+/*
+ * Read and clear the current device's error word (synchronous).  Kernels
+ * that wait on on-chip barriers give up after a bounded time instead of
+ * hanging, set a nonzero code here and exit; *code receives 0 if nothing
+ * went wrong since the last read.
+ */
+int tf_device_error(unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TF_H_ */

@@ -1,0 +1,129 @@
+"""Host-side tests of libtf through its C ABI (no GPU needed).
+
+The library must load and export every function include/tf.h declares; the
+C++ pre-tiling must produce exactly the blob the reference layout defines;
+its inverse must be exact; invalid arguments must come back as status codes.
+"""
+
+import ctypes
+import subprocess
+
+import numpy as np
+import pytest
+
+import gemv_tf_prepack_gb300 as tf
+from gemv_tf_prepack_gb300 import synth
+from oracle import layout as L
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    from gemv_tf_prepack_gb300 import build as b
+    b.build()
+    return tf.lib()
+
+
+def test_exports_every_declared_symbol():
+    decl = tf.header_declarations()
+    assert len(decl) >= 11
+    out = subprocess.run(["nm", "-D", "--defined-only", tf.lib_path], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [d for d in decl if d not in exported]
+    assert not missing, missing
+    lib = tf.lib()
+    for d in decl:
+        getattr(lib, d)
+    assert tf.version() == 1
+
+
+@pytest.mark.parametrize("N,K,bits,group", [
+    (256, 512, 4, 128), (200, 192, 4, 64), (136, 200, 8, 0), (64, 96, 4, 32),
+    (130, 256, 8, 128), (8, 8, 4, 0), (128, 1024, 4, 256), (300, 384, 8, 64), (72, 96, 8, 32),
+])
+def test_prepack_matches_reference_layout(N, K, bits, group):
+    qw = synth.make_weights(N, K, bits, group, 5)
+    ref = L.prepack(qw.qweight, qw.scales, qw.zeros, N, K, bits, group)
+    got = tf.prepack(qw.qweight, qw.scales, qw.zeros, N, K, bits, group)
+    assert got.size == ref.size == tf.prepack_size(N, K, bits, group)
+    np.testing.assert_array_equal(got, ref)
+    qw2, s2, z2, n2, k2, b2, g2 = tf.unprepack(got)
+    assert (n2, k2, b2, g2) == (N, K, bits, group)
+    np.testing.assert_array_equal(qw2, qw.qweight)
+    np.testing.assert_array_equal(s2, qw.scales)
+    np.testing.assert_array_equal(z2, qw.zeros)
+
+
+def test_prepack_decode_shape_round_trip():
+    N, K = 4096, 4096
+    qw = synth.make_weights(N, K, 4, 128, 2)
+    blob = tf.prepack(qw.qweight, qw.scales, qw.zeros, N, K, 4, 128)
+    r = tf.unprepack(blob)
+    np.testing.assert_array_equal(r[0], qw.qweight)
+    np.testing.assert_array_equal(r[1], qw.scales)
+    np.testing.assert_array_equal(r[2], qw.zeros)
+
+
+def test_prepack_sizes():
+    assert tf.prepack_size(32768, 32768, 4, 128) == 64 + 65536 * 8512
+    assert tf.prepack_size(8192, 8192, 8, 0) == 64 + 64 * 64 * 16768
+    assert tf.prepack_size(4096, 4096, 4, 64) == 64 + 32 * 32 * 8832
+
+
+def _rc(fn, *args):
+    return fn(*args)
+
+
+def test_invalid_arguments_return_codes():
+    lib = tf.lib()
+    sz = ctypes.c_size_t()
+    assert lib.tf_prepack_size(0, 128, 4, 128, ctypes.byref(sz)) == -1
+    assert lib.tf_prepack_size(128, 100, 4, 0, ctypes.byref(sz)) == -1       # K % 8
+    assert lib.tf_prepack_size(128, 256, 4, 96, ctypes.byref(sz)) == -2      # group 96
+    assert lib.tf_prepack_size(128, 192, 4, 128, ctypes.byref(sz)) == -1     # K % g
+    assert lib.tf_prepack_size(32769, 128, 4, 128, ctypes.byref(sz)) == -2   # > 32K
+    assert lib.tf_prepack_size(128, 128, 3, 128, ctypes.byref(sz)) == -2     # bits
+    assert lib.tf_prepack_size(32768, 32768, 8, 0, ctypes.byref(sz)) == 0
+    assert lib.tf_prepack_size(128, 128, 4, 128, None) == -1
+    # zeros out of range for INT4
+    qw = np.zeros((8, 16), np.uint32)
+    s = np.zeros((8, 1), np.uint16)
+    z = np.full((8, 1), 16, np.uint8)
+    out = np.zeros(tf.prepack_size(8, 128, 4, 128), np.uint8)
+    assert lib.tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, 8, 128, 4, 128,
+                          out.ctypes.data, out.size) == -1
+    assert lib.tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, 8, 128, 4, 128,
+                          out.ctypes.data, out.size - 1) == -1
+    # corrupted header
+    z[:] = 3
+    assert lib.tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, 8, 128, 4, 128,
+                          out.ctypes.data, out.size) == 0
+    bad = out.copy()
+    bad[0] ^= 1
+    with pytest.raises(tf.TFError) as e:
+        tf.unprepack(bad)
+    assert e.value.status == -5
+    short = out[:-16]
+    with pytest.raises(tf.TFError):
+        tf.unprepack(short)
+    for code in range(-7, 1):
+        assert lib.tf_status_string(code)
+
+
+def test_device_calls_validate_before_touching_the_gpu():
+    """Argument errors are reported without any CUDA call."""
+    lib = tf.lib()
+    blob = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    size = tf.prepack_size(256, 512, 4, 128)
+    x = ctypes.c_void_p(8192)
+    y = ctypes.c_void_p(16384)
+    # wrong blob size
+    assert lib.tf_gemv(blob, size - 16, 256, 512, 4, 128, x, y, 1, None, 0, None) == -5
+    # misaligned blob
+    assert lib.tf_gemv(ctypes.c_void_p(4100), size, 256, 512, 4, 128, x, y, 1, None, 0, None) == -3
+    # M out of range
+    assert lib.tf_gemv(blob, size, 256, 512, 4, 128, x, y, 9, None, 0, None) == -2
+    assert lib.tf_gemv(blob, size, 256, 512, 4, 128, x, y, 0, None, 0, None) == -1
+    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 0, None) == -1
+    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, ctypes.c_void_p(8194), y, 4, None) == -3
+    assert lib.tf_dequant(None, size, 256, 512, 4, 128, y, None) == -1
+    assert lib.tf_dequant(blob, size, 256, 512, 4, 96, y, None) == -2
