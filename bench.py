@@ -1,0 +1,476 @@
+"""Benchmark of the fused INT4/INT8-weight linear layer on GB300.
+
+Default run (N=1): the decode step of a Llama-7B-like layer — the four W4A16
+g128 projections (12288x4096 fused QKV, 4096x4096 O, 22016x4096 fused
+gate/up, 4096x11008 down) at M=1 through tf_gemv — reported as HBM GB/s of
+algorithmic bytes; in the same run the prefill GEMMs (11008x4096, 4096x11008,
+12288x4096 at M=2048 with 1% outlier activation columns) through tf_gemm,
+reported as TFLOP/s.  Inputs are seeded synthetic weights quantised with the
+AWQ-style min/max recipe and BF16 activations.
+
+Timing: W untimed warm-up steps, then K steps replayed from CUDA graphs on
+one stream, bracketed by CUDA events with a device synchronisation on both
+sides; the GEMV step rotates through weight copies totalling more than 3x
+the L2 size so that every launch streams its weights from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "W4A16 GEMV HBM GB/s (% of ~8 TB/s); prefill GEMM TFLOP/s (% BF16 peak)"
+DECODE = [(12288, 4096, 1), (4096, 4096, 2), (22016, 4096, 3), (4096, 11008, 4)]  # (N, K, seed)
+PREFILL = [(11008, 4096, 7), (4096, 11008, 8), (12288, 4096, 9)]
+PREFILL_M = 2048
+BITS, GROUP = 4, 128
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algo_bytes(M, N, K, bits=BITS, group=GROUP):
+    """Weights + one BF16 scale and one b-bit zero per group + x + y."""
+    g = K if group == 0 else group
+    return N * K * bits / 8 + (N * K / g) * (2 + bits / 8) + 2 * M * K + 2 * M * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+GEMV_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemv.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
+                "gemv_tf_prepack_gb300/csrc/tf_format.h"]
+GEMM_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemm.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
+                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
+
+
+def recorded_traffic(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = source_hash(sources)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
+                return float(parts[1]) if parts[2] == want else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.flush()
+
+    def summary(self):
+        self.tmp.seek(0)
+        rows = [r.split(", ") for r in self.tmp.read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def build_layers(torch, tf, synth, shapes, M, outliers, copies):
+    layers = []
+    for (N, K, seed) in shapes:
+        qw = synth.make_weights(N, K, BITS, GROUP, seed)
+        blob = tf.prepack(qw.qweight, qw.scales, qw.zeros, N, K, BITS, GROUP)
+        Ws = [tf.Weights.upload(blob) for _ in range(copies)]
+        xb = synth.make_activations(M, K, seed, outliers=outliers)
+        xh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+        layers.append(dict(N=N, K=K, Ws=Ws, x_host=xh,
+                           xs=[xh.cuda() for _ in range(copies)],
+                           ys=[torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]))
+    return layers
+
+
+def timing_event(torch):
+    """An event that becomes a real record node when captured in a CUDA graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # older torch: no external events
+        return None
+
+
+def capture_step(torch, fn, layers, r, stream, events):
+    """CUDA graph of one step on copy r, with an event between consecutive launches."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        if events[0] is not None:
+            events[0].record(stream)
+        for i, L in enumerate(layers):
+            fn(L["Ws"][r], L["xs"][r], L["ys"][r])
+            if events[i + 1] is not None:
+                events[i + 1].record(stream)
+    return g
+
+
+def launch_times(torch, ev, ncopies, layers, fn, stream):
+    """Per-launch durations (ms) from the events captured in the step graphs.
+
+    Without external graph events (older torch) the launches are timed with
+    eager events on the same stream instead.
+    """
+    if ev[0][0] is not None:
+        return [ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(ncopies) for i in range(len(layers))]
+    out = []
+    for r in range(ncopies):
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(len(layers) + 1)]
+        with torch.cuda.stream(stream):
+            es[0].record(stream)
+            for i, L in enumerate(layers):
+                fn(L["Ws"][r], L["xs"][r], L["ys"][r])
+                es[i + 1].record(stream)
+        torch.cuda.synchronize()
+        out += [es[i].elapsed_time(es[i + 1]) for i in range(len(layers))]
+    return out
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import gemv_tf_prepack_gb300 as tf
+    from gemv_tf_prepack_gb300 import synth
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, tc_peak_sus, peak_src = peaks()
+    stream = torch.cuda.Stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------- decode GEMV step (headline value) ----------------
+    step_bytes = sum(algo_bytes(1, N, K) for N, K, _ in DECODE)
+    blob_bytes = sum(tf.prepack_size(N, K, BITS, GROUP) for N, K, _ in DECODE)
+    copies = max(4, int(np.ceil(3 * L2_BYTES / blob_bytes)) + 1)
+    dec = build_layers(torch, tf, synth, DECODE, 1, False, copies)
+    for L in dec:
+        for W in L["Ws"]:
+            W.workspace(1)  # allocate (zero-filled) outside the graphs
+
+    def gemv_call(W, x, y):
+        tf.gemv(W, x, y, stream=stream)
+
+    ev = [[timing_event(torch) for _ in range(len(DECODE) + 1)] for _ in range(copies)]
+    with torch.cuda.stream(stream):
+        for r in range(copies):  # warm the lazy paths before capture
+            for L in dec:
+                gemv_call(L["Ws"][r], L["xs"][r], L["ys"][r])
+    torch.cuda.synchronize()
+    graphs = [capture_step(torch, gemv_call, dec, r, stream, ev[r]) for r in range(copies)]
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for s in range(args.warmup):
+            graphs[s % copies].replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk, torch.cuda.stream(stream):
+        t0.record(stream)
+        for s in range(args.steps):
+            graphs[s % copies].replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_step = max_over_ranks(t0.elapsed_time(t1) / args.steps)
+    clocks = clk.summary()
+    # per-launch kernel time: the last replay of every copy inside the timed region
+    k_ms = launch_times(torch, ev, min(copies, args.steps), dec, gemv_call, stream)
+    kernel_ms = sum(k_ms) / len(k_ms)
+    per_launch_bytes = step_bytes / len(DECODE)
+    achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---------------- end to end through the public API (host buffers) ----------------
+    x_pin = [L["x_host"].pin_memory() for L in dec]
+    y_pin = [torch.empty((1, L["N"]), dtype=torch.bfloat16).pin_memory() for L in dec]
+    h2d = sum(x.numel() * 2 for x in x_pin)
+    d2h = sum(y.numel() * 2 for y in y_pin)
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup + e2e_steps):
+            if s == args.warmup:
+                torch.cuda.synchronize()
+                barrier()
+                te = time.perf_counter()
+            r = s % copies
+            for i, L in enumerate(dec):
+                L["xs"][r].copy_(x_pin[i], non_blocking=True)
+                tf.gemv(L["Ws"][r], L["xs"][r], L["ys"][r], stream=stream)
+                y_pin[i].copy_(L["ys"][r], non_blocking=True)
+            stream.synchronize()
+    e2e_ms = max_over_ranks((time.perf_counter() - te) * 1e3 / e2e_steps)
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    # ---------------- prefill GEMM (M=2048) ----------------
+    for L in dec:
+        L["Ws"].clear(); L["xs"].clear(); L["ys"].clear()
+    del graphs
+    torch.cuda.empty_cache()
+    pcopies = 2
+    pre = build_layers(torch, tf, synth, PREFILL, PREFILL_M, True, pcopies)
+
+    def gemm_call(W, x, y):
+        tf.gemm(W, x, y, stream=stream)
+
+    pev = [[timing_event(torch) for _ in range(len(PREFILL) + 1)] for _ in range(pcopies)]
+    with torch.cuda.stream(stream):
+        for r in range(pcopies):
+            for L in pre:
+                gemm_call(L["Ws"][r], L["xs"][r], L["ys"][r])
+    torch.cuda.synchronize()
+    pgraphs = [capture_step(torch, gemm_call, pre, r, stream, pev[r]) for r in range(pcopies)]
+    psteps = max(args.steps // 20, 10)
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            pgraphs[s % pcopies].replay()
+    torch.cuda.synchronize()
+    barrier()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as pclk, torch.cuda.stream(stream):
+        p0.record(stream)
+        for s in range(psteps):
+            pgraphs[s % pcopies].replay()
+        p1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    pms = max_over_ranks(p0.elapsed_time(p1) / psteps)
+    pk = launch_times(torch, pev, pcopies, pre, gemm_call, stream)
+    flops = sum(2.0 * PREFILL_M * N * K for N, K, _ in PREFILL)
+    p_kernel_ms = sum(pk) / len(pk)
+    p_achieved = flops / len(PREFILL) / (p_kernel_ms * 1e-3) / 1e12
+    prefill_tflops = world * flops / (pms * 1e-3) / 1e12
+    long_region = pms * psteps > 1000.0
+    tc_ref = tc_peak_sus if long_region else tc_peak
+    pclocks = pclk.summary()
+
+    err = tf.device_error()
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, AWQ-style min/max W4 g128 quantisation; BF16 N(0,1) activations)",
+        "config": {
+            "workload": "decode step: 4 Llama-7B-like W4A16 g128 projections (12288x4096, 4096x4096, "
+                        "22016x4096, 4096x11008) at M=1 through tf_gemv",
+            "l2": f"rotates {copies} weight copies ({copies * blob_bytes / 1e6:.0f} MB > 3x L2) via CUDA graphs",
+            "parallelism": f"replicas x{world}",
+            "hbm_pct_of_8tbs": round(100 * value / world / 8000.0, 1),
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+            "traffic": recorded_traffic("gemv_kernel", GEMV_SOURCES),
+            "kernel": "gemv_kernel<4,1,4>", "algorithmic_bytes_per_launch": round(per_launch_bytes),
+            "kernel_us_per_launch": round(kernel_ms * 1e3, 3),
+        },
+        "prefill": {
+            "workload": "W4A16 g128 GEMM at M=2048 (11008x4096, 4096x11008, 12288x4096), 1% outlier columns",
+            "value": round(prefill_tflops, 1), "unit": "TFLOP/s", "ms_per_step": round(pms, 4),
+            "roofline": {"bound": "tensor", "achieved": round(p_achieved, 1), "peak": tc_ref, "unit": "TFLOP/s",
+                         "frac": round(p_achieved / tc_ref, 4), "peak_source": peak_src + (
+                             " sustained" if long_region else " burst"),
+                         "traffic": recorded_traffic("gemm_kernel", GEMM_SOURCES),
+                         "kernel": "gemm_kernel<4,1>"},
+            "clocks": pclocks,
+            "gpu_launches": psteps * len(PREFILL),
+        },
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "path": "pinned host x -> device, tf_gemv x4 through the Python binding, y -> pinned host"},
+        "gpu_launches": args.steps * len(DECODE),
+        "clocks": clocks,
+        "device_error": err,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+
+CPU_SAMPLE_ROWS = 256
+
+
+def _oracle_sample_cmd():
+    return [sys.executable, os.path.abspath(__file__), "--oracle-sample"]
+
+
+def oracle_sample() -> dict:
+    """Time the oracle on the first 256 output rows of each decode projection."""
+    from gemv_tf_prepack_gb300 import synth
+    from oracle import tf_oracle
+
+    data = []
+    for N, K, seed in DECODE:
+        rng = np.random.default_rng(seed)
+        w = rng.standard_normal((CPU_SAMPLE_ROWS, K), dtype=np.float32) * np.float32(0.02)
+        qw = synth.quantise(w, BITS, GROUP)
+        data.append((qw, synth.make_activations(1, K, seed)))
+    t = time.perf_counter()
+    for qw, x in data:
+        tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, BITS, GROUP, qw.K, x)
+    dt = time.perf_counter() - t
+    nbytes = sum(algo_bytes(1, CPU_SAMPLE_ROWS, qw.K) for qw, _ in data)
+    return {"seconds": dt, "bytes": nbytes}
+
+
+def cpu_baseline(reps: int = 1) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    secs, nbytes = 0.0, 0.0
+    for _ in range(reps):
+        out = subprocess.run(_oracle_sample_cmd(), capture_output=True, text=True, env=env, cwd=ROOT)
+        rec = json.loads(out.stdout.strip().splitlines()[-1])
+        secs += rec["seconds"]
+        nbytes += rec["bytes"]
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"unpack + dequant + float64 product of the first {CPU_SAMPLE_ROWS} output rows of each "
+                      "of the 4 decode projections (M=1), one process, BLAS threads = 1"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    times, nbytes = [], None
+    for s in range(args.warmup + args.steps):
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+            env.pop(k, None)
+        out = subprocess.run(_oracle_sample_cmd(), capture_output=True, text=True, env=env, cwd=ROOT)
+        rec = json.loads(out.stdout.strip().splitlines()[-1])
+        if s >= args.warmup:
+            times.append(rec["seconds"])
+            nbytes = rec["bytes"]
+    sec = sum(times) / len(times)
+    value = nbytes / sec / 1e9
+    sample = (f"oracle (float64 CPU reference): first {CPU_SAMPLE_ROWS} output rows of each of the 4 decode "
+              "projections per step, one process, BLAS threads = 1")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode step: 4 Llama-7B-like W4A16 g128 projections at M=1 (row sample)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_sample:
+        print(json.dumps(oracle_sample()))
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,10 +22,9 @@
 // SM) and walk output tiles with the token index fastest, so CTAs that run
 // together share weight tiles in L2.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "../../include/tf.h"
 #include "tf_abi.h"
@@ -34,9 +33,6 @@
 #include "tf_sm100.cuh"
 
 namespace tf {
-
-// Device-side error word (first error wins); read by tf_device_error.
-__device__ unsigned g_tf_error;
 
 namespace {
 
@@ -58,6 +54,7 @@ enum : unsigned {
 struct GemmArgs {
   const uint8_t* tiles;
   uint16_t* y;
+  unsigned* err;              // device error word
   int N, K, M, KT, g, tile_bytes;
   int MT, BN, ntiles;
   int P, OPS;                 // stages of the packed ring and of the operand ring
@@ -91,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const Bars B = bars_at(sbase + a.off_bar, a.P, a.OPS);
   const uint32_t x_slab_bytes = (uint32_t)a.BN * 128;
   const uint32_t op_stage_bytes = kSlabBytesW + x_slab_bytes;
-  unsigned* err = &g_tf_error;
+  unsigned* err = a.err;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.P; ++i) {
@@ -219,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else {
     // ---------------------------------------------------------------- dequant
     const int mb = warp - kDequantWarp0;  // 16-row block of every tile
-    const int gr = lane & 7, t = lane >> 3;  // lane reads slot p = lane (conflict-free)
+    const int gr = lane >> 2, t = lane & 3;  // lane reads slot p = lane (conflict-free)
     constexpr int WB = kTileN * kTileK * BITS / 8;
     constexpr int SB = BITS == 4 ? 16 : 32;
     constexpr int ZB = BITS == 4 ? 64 : 128;
@@ -303,20 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // ---------------------------------------------------------------------------
 // host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmPlan {
@@ -354,9 +337,15 @@ int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
 template <int BITS, int GPT>
 int launch_gemm(const CUtensorMap& map, const GemmPlan& P, cudaStream_t s) {
   auto kfn = gemm_kernel<BITS, GPT>;
-  // The attribute is per function; setting it is cheap and thread-safe.
-  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem) != cudaSuccess)
-    return TF_ERR_CUDA;
+  // Opt in once per device to the largest shared-memory carve-out.
+  static std::atomic<unsigned long long> opted{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
+  if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+      return TF_ERR_CUDA;
+    opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
   kfn<<<P.grid, kThreads, P.smem, s>>>(map, P.a);
   return launch_status();
 }
@@ -380,17 +369,11 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   if (rc) return rc;
   P.a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   P.a.y = y;
-  auto enc = encode_fn();
-  if (!enc) return TF_ERR_CUDA;
+  P.a.err = device_error_ptr();
+  if (!P.a.err) return TF_ERR_CUDA;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)P.a.BN};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return TF_ERR_CUDA;
+  rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
+  if (rc) return rc;
   if (bits == 4) {
     if (G.gpt == 1) return launch_gemm<4, 1>(map, P, stream);
     if (G.gpt == 2) return launch_gemm<4, 2>(map, P, stream);
@@ -399,15 +382,6 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   if (G.gpt == 1) return launch_gemm<8, 1>(map, P, stream);
   if (G.gpt == 2) return launch_gemm<8, 2>(map, P, stream);
   return launch_gemm<8, 4>(map, P, stream);
-}
-
-int tf_device_error(unsigned int* code) {
-  if (!code) return TF_ERR_INVALID_ARG;
-  unsigned v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, g_tf_error, sizeof v) != cudaSuccess) return TF_ERR_CUDA;
-  if (cudaMemcpyToSymbol(g_tf_error, &zero, sizeof zero) != cudaSuccess) return TF_ERR_CUDA;
-  *code = v;
-  return TF_OK;
 }
 
 }  // extern "C"

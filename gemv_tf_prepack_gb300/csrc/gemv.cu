@@ -11,10 +11,13 @@
 // multiply-accumulate instead of CUDA-core FMAs.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/tf.h"
 #include "tf_abi.h"
 #include "tf_device.cuh"
 #include "tf_format.h"
+#include "tf_sm100.cuh"
 
 namespace tf {
 namespace {
@@ -31,7 +34,7 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
   const int mb = threadIdx.x >> 6;
   const int h = (threadIdx.x >> 5) & 1;
   const int p = threadIdx.x & 31;
-  const int gr = p & 7, t = p >> 3;
+  const int gr = p >> 2, t = p & 3;
   constexpr int WB = kTileN * kTileK * BITS / 8;
   constexpr int SB = BITS == 4 ? 16 : 32;
   constexpr int ZB = BITS == 4 ? 64 : 128;
@@ -83,22 +86,39 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
 // tf_gemv
 //
 // Work split: the T = NB * KT tiles are numbered in blob order and CTA c
-// streams tiles [c*T/G, (c+1)*T/G): one contiguous byte range.  Warp w of a
-// CTA owns row block w (16 rows) of every tile in that range, so no
-// intra-CTA reduction is needed.  A CTA's range covers whole or partial
-// 128-row blocks ("segments"); a whole block is written straight to y, a
-// partial one is stored as FP32 fragments in the workspace and the last of
-// the block's contributors (arrival counter per row block) adds them in CTA
-// order — a fixed order, so the result does not depend on arrival order.
+// streams tiles [c*T/G, (c+1)*T/G) — one contiguous byte range, which a
+// shared-memory ring fetches with 1-D bulk copies (two tiles per stage), the
+// tiles' activation slices x[:, kt*128 : kt*128+128] arriving alongside by
+// 2-D TMA (zero-filled past K).  The warp that hands a stage back last
+// refills it, so no warp is dedicated to (or delayed by) producing.  Warp w
+// of the CTA owns row block w (16 rows) of every tile, so no intra-CTA
+// reduction is needed.  A
+// CTA's range covers whole or partial 128-row blocks ("segments"); a whole
+// block is written straight to y, a partial one is stored as FP32 fragments
+// in the workspace and the last of the block's contributors (arrival counter
+// per row block) adds them in CTA order — a fixed order, so the result does
+// not depend on arrival order.
+//
+// The kernel is launched with programmatic dependent launch: the weight
+// stream (static data) starts before the previous kernel on the stream has
+// finished; activations, y and the workspace are touched only after it has.
+
+constexpr int kGemvConsumers = 8;                  // one warp per 16-row block
+// tiles per ring stage (one bulk copy)
+__host__ __device__ constexpr int tiles_per_stage(int) { return 2; }
+constexpr int kGemvThreads = 32 * kGemvConsumers;
+constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
+constexpr unsigned kErrGemvWait = 0x600;
 
 struct GemvArgs {
   const uint8_t* tiles;
-  const uint16_t* x;
   uint16_t* y;
   float4* partials;    // [G][S_max][8 warps][32 lanes]
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
+  unsigned* err;
   long long T;
   int N, K, M, KT, g, tile_bytes, G, S_max;
+  int NS, stage_bytes, x_off;  // shared-memory ring: stages, bytes per stage, x slice offset
 };
 
 __device__ __forceinline__ long long tile_begin(long long c, long long T, int G) { return c * T / G; }
@@ -106,30 +126,6 @@ __device__ __forceinline__ long long tile_begin(long long c, long long T, int G)
 // CTA whose range holds tile x.
 __device__ __forceinline__ int cta_of_tile(long long x, long long T, int G) {
   return (int)(((x + 1) * G - 1) / T);
-}
-
-template <int BITS, int GPT>
-struct Stage {
-  uint4 w[2][BITS == 4 ? 1 : 2];  // this lane's slot in quad 0 and quad 1
-  uint32_t s[GPT == 1 ? 1 : 2];   // scale pair per quad
-  uint32_t z[GPT == 1 ? 1 : 2];   // zero byte(s) per quad
-};
-
-template <int BITS, int GPT>
-__device__ __forceinline__ void load_stage(Stage<BITS, GPT>& S, const uint8_t* tb, int woff, int soff,
-                                           int zoff, int gi0, int gi1) {
-  constexpr int SB = BITS == 4 ? 16 : 32;
-  constexpr int ZB = BITS == 4 ? 64 : 128;
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int v = 0; v < SB / 16; ++v) S.w[h][v] = ld_stream_v4(tb + woff + h * 32 * SB + v * 16);
-  S.s[0] = ld_stream_u32(tb + soff + gi0 * 256);
-  S.z[0] = BITS == 4 ? ld_stream_u8(tb + zoff + gi0 * ZB) : ld_stream_u16(tb + zoff + gi0 * ZB);
-  if (GPT > 1) {
-    S.s[GPT == 1 ? 0 : 1] = ld_stream_u32(tb + soff + gi1 * 256);
-    S.z[GPT == 1 ? 0 : 1] = BITS == 4 ? ld_stream_u8(tb + zoff + gi1 * ZB) : ld_stream_u16(tb + zoff + gi1 * ZB);
-  }
 }
 
 __device__ __forceinline__ void store_y(const GemvArgs& a, int n0, int t, const float (&v)[4]) {
@@ -176,106 +172,235 @@ __device__ __forceinline__ void flush_segment(const GemvArgs& a, int c, long lon
   if (lane == 0) a.counters[nb * 8 + warp] = 0u;
 }
 
-template <int BITS, int GPT, int D>
-__global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t = lane & 3;  // mma.sync fragment coordinates
-  const int p = 8 * t + gr;                // this lane's slot in a (row block, quad)
-  const int c = blockIdx.x;
-  const long long t0 = tile_begin(c, a.T, a.G), t1 = tile_begin(c + 1, a.T, a.G);
-  if (t0 >= t1) return;
+// Registers of one tile for one consumer lane: its weight slot in both K
+// quads, the activation fragments and the tile's scale / zero words.
+template <int BITS, int GPT>
+struct TileRegs {
+  uint4 w[2][BITS == 4 ? 1 : 2];
+  uint4 x[2][2];
+  uint32_t sp[GPT == 1 ? 1 : 2], zp[GPT == 1 ? 1 : 2];
+};
 
+struct LaneOffsets {
+  int w, s, z, x, gi0, gi1;
+};
+
+template <int BITS, int GPT>
+__device__ __forceinline__ void load_tile(TileRegs<BITS, GPT>& R, const uint8_t* tb, const uint8_t* xb,
+                                          const LaneOffsets& o) {
   constexpr int SB = BITS == 4 ? 16 : 32;
-  constexpr int WB = kTileN * kTileK * BITS / 8;
-  const int woff = warp * 2 * 32 * SB + p * SB;
-  const int soff = WB + (warp * 8 + gr) * 4;
-  const int zoff = WB + GPT * 256 + (BITS == 4 ? (warp * 8 + gr) : (warp * 8 + gr) * 2);
-  const int gi0 = GPT == 1 ? 0 : (16 * t) / a.g;
-  const int gi1 = GPT == 1 ? 0 : (64 + 16 * t) / a.g;
+  constexpr int ZB = BITS == 4 ? 64 : 128;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int v = 0; v < SB / 16; ++v) R.w[h][v] = *reinterpret_cast<const uint4*>(tb + o.w + h * 32 * SB + v * 16);
+    R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
+    R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
+  }
+  R.sp[0] = *reinterpret_cast<const uint32_t*>(tb + o.s + o.gi0 * 256);
+  R.zp[0] = BITS == 4 ? (uint32_t)tb[o.z + o.gi0 * ZB] : (uint32_t)*reinterpret_cast<const uint16_t*>(tb + o.z + o.gi0 * ZB);
+  if (GPT > 1) {
+    R.sp[GPT == 1 ? 0 : 1] = *reinterpret_cast<const uint32_t*>(tb + o.s + o.gi1 * 256);
+    R.zp[GPT == 1 ? 0 : 1] = BITS == 4 ? (uint32_t)tb[o.z + o.gi1 * ZB]
+                                        : (uint32_t)*reinterpret_cast<const uint16_t*>(tb + o.z + o.gi1 * ZB);
+  }
+}
 
-  Stage<BITS, GPT> st[D];
+// Unpack, dequantise (bit-exact BF16) and multiply-accumulate one tile.
+template <int BITS, int GPT>
+__device__ __forceinline__ void mma_tile(const TileRegs<BITS, GPT>& R, float (&acc)[2][4]) {
 #pragma unroll
-  for (int s = 0; s < D; ++s)
-    if (t0 + s < t1) load_stage(st[s], a.tiles + (t0 + s) * a.tile_bytes, woff, soff, zoff, gi0, gi1);
-
-  const bool x_active = gr < a.M;
-  const uint16_t* xrow = a.x + (size_t)(x_active ? gr : 0) * a.K;
-
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  int nb = (int)(t0 / a.KT);
-  int kt = (int)(t0 - (long long)nb * a.KT);
-  bool seg_whole = kt == 0;
-
-  for (long long base = t0; base < t1; base += D) {
+  for (int h = 0; h < 2; ++h) {
+    const int mi = GPT == 1 ? 0 : h;
+    const uint32_t xs[8] = {R.x[h][0].x, R.x[h][0].y, R.x[h][0].z, R.x[h][0].w,
+                            R.x[h][1].x, R.x[h][1].y, R.x[h][1].z, R.x[h][1].w};
+    if (BITS == 4) {
+      const MetaW4 m = meta_w4(R.sp[mi], R.zp[mi]);
+      const uint32_t words[4] = {R.w[h][0].x, R.w[h][0].y, R.w[h][0].z, R.w[h][0].w};
 #pragma unroll
-    for (int s = 0; s < D; ++s) {
-      const long long tau = base + s;
-      if (tau < t1) {
-        // activations for this tile: x[gr, k0 .. k0+15] per quad
-        uint32_t xs[2][8];
+      for (int j = 0; j < 4; ++j) {
+        uint32_t af[4];
+        dequant_w4(words[j], m, af);
+        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
+      }
+    } else {
+      const MetaW8 m = meta_w8(R.sp[mi], R.zp[mi]);
+      const uint4 v0 = R.w[h][0], v1 = R.w[h][BITS == 4 ? 0 : 1];
+      const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int k0 = kt * kTileK + h * 64 + 16 * t;
-          uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-          if (x_active && k0 < a.K) v0 = ld_keep_v4(xrow + k0);
-          if (x_active && k0 + 8 < a.K) v1 = ld_keep_v4(xrow + k0 + 8);
-          xs[h][0] = v0.x; xs[h][1] = v0.y; xs[h][2] = v0.z; xs[h][3] = v0.w;
-          xs[h][4] = v1.x; xs[h][5] = v1.y; xs[h][6] = v1.z; xs[h][7] = v1.w;
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int mi = GPT == 1 ? 0 : h;
-          if (BITS == 4) {
-            const MetaW4 m = meta_w4(st[s].s[mi], st[s].z[mi]);
-            const uint4 v = st[s].w[h][0];
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t af[4];
-              dequant_w4(words[j], m, af);
-              mma_16816(acc[h], af, xs[h][2 * j], xs[h][2 * j + 1]);
-            }
-          } else {
-            const MetaW8 m = meta_w8(st[s].s[mi], st[s].z[mi]);
-            const uint4 v0 = st[s].w[h][0], v1 = st[s].w[h][BITS == 4 ? 0 : 1];
-            const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t af[4];
-              dequant_w8(words[2 * j], words[2 * j + 1], m, af);
-              mma_16816(acc[h], af, xs[h][2 * j], xs[h][2 * j + 1]);
-            }
-          }
-        }
-        if (tau + D < t1) load_stage(st[s], a.tiles + (tau + D) * a.tile_bytes, woff, soff, zoff, gi0, gi1);
-
-        if (kt == a.KT - 1 || tau == t1 - 1) {
-          const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
-                              acc[0][3] + acc[1][3]};
-          flush_segment(a, c, t0, nb, seg_whole && kt == a.KT - 1, warp, lane, v);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[h][i] = 0.f;
-          seg_whole = true;
-          kt = 0;
-          ++nb;
-        } else {
-          ++kt;
-        }
+      for (int j = 0; j < 4; ++j) {
+        uint32_t af[4];
+        dequant_w8(words[2 * j], words[2 * j + 1], m, af);
+        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
       }
     }
   }
 }
 
-// Grid of the GEMV: two 256-thread CTAs per SM, never more CTAs than tiles.
+// Segment bookkeeping of one consumer warp: local index of the segment's
+// last tile, whether the segment covers its whole row block, and the block.
+struct Segment {
+  int end, nb;
+  bool whole;
+};
+
+__device__ __forceinline__ Segment first_segment(long long t0, int ntile, int KT) {
+  Segment g;
+  g.nb = (int)(t0 / KT);
+  const int kt0 = (int)(t0 - (long long)g.nb * KT);
+  const int len = KT - kt0;
+  g.end = (len < ntile ? len : ntile) - 1;
+  g.whole = kt0 == 0 && len <= ntile;
+  return g;
+}
+
+__device__ __forceinline__ void next_segment(Segment& g, int ntile, int KT) {
+  const int start = g.end + 1;
+  const int left = ntile - start;
+  g.end = start + (KT < left ? KT : left) - 1;
+  g.whole = KT <= left;
+  ++g.nb;
+}
+
+// Issue fill f of this CTA's ring (tiles 2f, 2f+1 of its range and their
+// activation slices) into slot s.  The activations are read only once the
+// grid dependency has resolved (x_ok).
+template <int TPS>
+__device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap* tmx, uint32_t sbase, uint32_t full,
+                                           long long t0, int ntile, int f, int s, bool weights, bool x) {
+  const int i = f * TPS;
+  const int n = ntile - i < TPS ? ntile - i : TPS;
+  const uint32_t x_bytes = (uint32_t)a.M * 256u;
+  const uint32_t bar = full + 8u * s;
+  const uint32_t dst = sbase + (uint32_t)(s * a.stage_bytes);
+  if (weights) {
+    mbar_arrive_expect_tx(bar, (uint32_t)n * ((uint32_t)a.tile_bytes + x_bytes));
+    bulk_load(dst, a.tiles + (t0 + i) * a.tile_bytes, (uint32_t)(n * a.tile_bytes), bar);
+  }
+  if (x) {
+    for (int q = 0; q < n; ++q) {
+      const int kt = (int)((t0 + i + q) % a.KT);
+      tma_load_2d(dst + (uint32_t)a.x_off + (uint32_t)q * x_bytes, tmx, kt * kTileK, 0, bar);
+    }
+  }
+}
+
+template <int BITS, int GPT>
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                               const GemvArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const long long t0 = tile_begin(c, a.T, a.G), t1 = tile_begin(c + 1, a.T, a.G);
+  const int ntile = (int)(t1 - t0);
+  constexpr int kTilesPerStage = tiles_per_stage(BITS);
+  const int nfill = (ntile + kTilesPerStage - 1) / kTilesPerStage;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full = sbase + (uint32_t)(a.NS * a.stage_bytes);
+  const uint32_t empty = full + 8u * a.NS;
+  // per-slot release counters: the last warp to hand a slot back refills it
+  unsigned* released = reinterpret_cast<unsigned*>(smem + a.NS * a.stage_bytes + 16 * a.NS);
+  const int npre = nfill < a.NS ? nfill : a.NS;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.NS; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(empty + 8 * i, kGemvConsumers);
+      released[i] = 0;
+    }
+    mbar_init_fence();
+    if (ntile > 0) {
+      griddep_launch_dependents();
+      prefetch_tensormap(&tmx);
+      // static weights first, before the grid dependency resolves
+      for (int f = 0; f < npre; ++f) issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, true, false);
+    }
+  }
+  __syncthreads();
+  if (ntile <= 0) return;
+  // y, x and the workspace may still be in use by the previous grid
+  griddep_wait();
+  if (threadIdx.x == 0)
+    for (int f = 0; f < npre; ++f) issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true);
+
+  const int gr = lane >> 2, t = lane & 3;  // mma.sync fragment coordinates
+  constexpr int SB = BITS == 4 ? 16 : 32;
+  constexpr int WB = kTileN * kTileK * BITS / 8;
+  LaneOffsets o;
+  o.w = warp * 2 * 32 * SB + lane * SB;  // slot p = 4 gr + t = lane
+  o.s = WB + (warp * 8 + gr) * 4;
+  o.z = WB + GPT * 256 + (BITS == 4 ? (warp * 8 + gr) : (warp * 8 + gr) * 2);
+  o.gi0 = GPT == 1 ? 0 : (16 * t) / a.g;
+  o.gi1 = GPT == 1 ? 0 : (64 + 16 * t) / a.g;
+  // Rows of B past M are never stored; those lanes read row M-1 again.
+  o.x = (gr < a.M ? gr : a.M - 1) * 256 + 32 * t;
+  const int x_stride = a.M * 256;
+
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  Segment seg = first_segment(t0, ntile, a.KT);
+  int s = 0;
+  uint32_t lap = 0;
+  for (int f = 0; f < nfill; ++f) {
+    if (!mbar_wait(full + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs)) break;
+    const int i0 = f * kTilesPerStage;
+    const uint8_t* st = smem + s * a.stage_bytes;
+    const uint8_t* xs = st + a.x_off;
+    const bool two = i0 + 1 < ntile;
+    TileRegs<BITS, GPT> A, B;
+    load_tile(A, st, xs, o);
+    if (two) load_tile(B, st + a.tile_bytes, xs + x_stride, o);
+    __syncwarp();
+    if (lane == 0) {
+      // the stage is in registers: hand it back; the last warp refills it
+      mbar_arrive(empty + 8 * s);
+      if (atomicAdd(released + s, 1u) == kGemvConsumers - 1) {
+        released[s] = 0;
+        if (f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs))
+          issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true);
+      }
+    }
+    __syncwarp();
+    if (++s == a.NS) { s = 0; ++lap; }
+
+    mma_tile(A, acc);
+    if (i0 == seg.end) {
+      const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]};
+      flush_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[h][q] = 0.f;
+      next_segment(seg, ntile, a.KT);
+    }
+    if (two) {
+      mma_tile(B, acc);
+      if (i0 + 1 == seg.end) {
+        const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
+                            acc[0][3] + acc[1][3]};
+        flush_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[h][q] = 0.f;
+        next_segment(seg, ntile, a.KT);
+      }
+    }
+  }
+}
+
+// Grid of the GEMV: two CTAs per SM, never more CTAs than tiles.
 struct GemvPlan {
   long long T;
   int G, S_max;
-  size_t partial_bytes, counter_bytes;
+  int NS, stage_bytes, x_off;
+  size_t smem, partial_bytes, counter_bytes;
 };
 
+constexpr int kGemvSmemBudget = 100 * 1024;  // ring bytes per CTA; two CTAs share an SM
+constexpr int kGemvSmemMax = 113 * 1024;
+
 inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
+  const int kTilesPerStage = tiles_per_stage(Gm.bits);
   const int sms = sm_count();
   if (sms <= 0) return TF_ERR_CUDA;
   P->T = (long long)Gm.NB * Gm.KT;
@@ -284,14 +409,43 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   P->S_max = (int)((per_cta + Gm.KT - 1) / Gm.KT + 1);
   P->partial_bytes = (size_t)P->G * P->S_max * 8 * 32 * sizeof(float4);
   P->counter_bytes = ((size_t)Gm.NB * 8 * sizeof(unsigned) + 255) / 256 * 256;
-  (void)M;
+  P->x_off = (kTilesPerStage * Gm.tile_bytes + 127) / 128 * 128;
+  P->stage_bytes = P->x_off + kTilesPerStage * M * 256;
+  int ns = kGemvSmemBudget / P->stage_bytes;
+  P->NS = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+  P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS;
   return TF_OK;
 }
 
 template <int BITS, int GPT>
-void launch_gemv(const GemvArgs& a, cudaStream_t s) {
-  constexpr int D = BITS == 4 ? 4 : 2;
-  gemv_kernel<BITS, GPT, D><<<a.G, 256, 0, s>>>(a);
+int launch_gemv(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
+  auto kfn = gemv_kernel<BITS, GPT>;
+  // Opt in once per device to the largest ring gemv_plan can ask for.
+  static std::atomic<unsigned long long> opted{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
+  if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return TF_ERR_CUDA;
+    opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+  if (smem > (size_t)kGemvSmemMax) return TF_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.G);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kfn, map, a) != cudaSuccess) {
+    cudaGetLastError();
+    return TF_ERR_CUDA;
+  }
+  return launch_status();
 }
 
 template <int BITS, int GPT>
@@ -352,25 +506,28 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
   if (!workspace || workspace_bytes < P.partial_bytes + P.counter_bytes) return TF_ERR_WORKSPACE;
+  CUtensorMap map;
+  rc = encode_x_map(x, M, K, &map);
+  if (rc) return rc;
   GemvArgs a;
   a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
-  a.x = x;
   a.y = y;
   a.partials = static_cast<float4*>(workspace);
   a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes);
+  a.err = device_error_ptr();
+  if (!a.err) return TF_ERR_CUDA;
   a.T = P.T;
   a.N = N; a.K = K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
   a.G = P.G; a.S_max = P.S_max;
+  a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
   if (bits == 4) {
-    if (G.gpt == 1) launch_gemv<4, 1>(a, stream);
-    else if (G.gpt == 2) launch_gemv<4, 2>(a, stream);
-    else launch_gemv<4, 4>(a, stream);
-  } else {
-    if (G.gpt == 1) launch_gemv<8, 1>(a, stream);
-    else if (G.gpt == 2) launch_gemv<8, 2>(a, stream);
-    else launch_gemv<8, 4>(a, stream);
+    if (G.gpt == 1) return launch_gemv<4, 1>(map, a, P.smem, stream);
+    if (G.gpt == 2) return launch_gemv<4, 2>(map, a, P.smem, stream);
+    return launch_gemv<4, 4>(map, a, P.smem, stream);
   }
-  return launch_status();
+  if (G.gpt == 1) return launch_gemv<8, 1>(map, a, P.smem, stream);
+  if (G.gpt == 2) return launch_gemv<8, 2>(map, a, P.smem, stream);
+  return launch_gemv<8, 4>(map, a, P.smem, stream);
 }
 
 }  // extern "C"

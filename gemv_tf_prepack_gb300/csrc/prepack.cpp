@@ -47,7 +47,7 @@ struct Source {
 
 // Tile row / column of code i of word j in slot p of block (mb, h).
 inline void code_position(int mb, int h, int p, int j, int i, int* row, int* col) {
-  const int gr = p & 7, t = p >> 3, r = i & 3, e = i >> 2;
+  const int gr = p >> 2, t = p & 3, r = i & 3, e = i >> 2;
   *row = mb * 16 + gr + 8 * (r & 1);
   *col = h * 64 + 16 * t + 4 * j + 2 * (r >> 1) + e;
 }

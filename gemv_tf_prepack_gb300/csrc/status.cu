@@ -1,0 +1,41 @@
+// The device-side error word of libtf and its host accessors.
+//
+// Kernels that wait on shared-memory barriers give up after a bounded time
+// instead of hanging; they then record a nonzero code here.  One word per
+// device, defined in this translation unit only; other units receive its
+// device address as a kernel argument.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "../../include/tf.h"
+#include "tf_abi.h"
+
+namespace tf {
+
+__device__ unsigned g_tf_error;
+
+unsigned* device_error_ptr() {
+  static std::atomic<unsigned*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+  if (dev < 64) {
+    unsigned* p = cache[dev].load(std::memory_order_acquire);
+    if (p) return p;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_tf_error) != cudaSuccess) return nullptr;
+  if (dev < 64) cache[dev].store(static_cast<unsigned*>(p), std::memory_order_release);
+  return static_cast<unsigned*>(p);
+}
+
+}  // namespace tf
+
+extern "C" int tf_device_error(unsigned int* code) {
+  if (!code) return TF_ERR_INVALID_ARG;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, tf::g_tf_error, sizeof v) != cudaSuccess) return TF_ERR_CUDA;
+  if (cudaMemcpyToSymbol(tf::g_tf_error, &zero, sizeof zero) != cudaSuccess) return TF_ERR_CUDA;
+  *code = v;
+  return TF_OK;
+}

@@ -1,6 +1,7 @@
 // Argument checks and device queries shared by the ABI entry points.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,6 +11,16 @@
 #include "tf_format.h"
 
 namespace tf {
+
+// Device address of the current device's error word (cached per device).
+unsigned* device_error_ptr();
+
+// TMA maps over the activations x [M, K] (BF16, row-major); columns past K
+// and rows past M read as zero.  encode_x_map: box of 128 columns x M rows,
+// no swizzle (one GEMV tile's slice).  encode_x_map_sw128: box of 64
+// columns x `rows` rows with the 128-byte swizzle (one GEMM operand slab).
+int encode_x_map(const uint16_t* x, int M, int K, CUtensorMap* map);
+int encode_x_map_sw128(const uint16_t* x, int M, int K, int rows, CUtensorMap* map);
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 

@@ -61,7 +61,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_timer_ns() - t0 > timeout_ns) {
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > timeout_ns) {
       atomicCAS(err, 0u, code);
       return false;
     }
@@ -94,6 +94,18 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // (tensor cores, TMA).
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch (no-ops unless the launch enables it)
+
+// Block until the grids this one depends on have completed and their memory
+// operations are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream to start launching.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

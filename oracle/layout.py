@@ -27,10 +27,11 @@ Tile = weights (128 * 128 * bits / 8 bytes), then scales, then zeros.
 
 Weights: 8 row blocks ``mb`` of 16 rows x 2 K-quads ``h`` of 64 columns; block
 ``(mb, h)`` starts at byte ``(mb * 2 + h) * 32 * P`` with ``P = 16`` (INT4) or
-32 (INT8) bytes per slot.  Slot ``p = 8 t + gr`` (``gr`` in 0..7, ``t`` in
-0..3) holds four words ``j = 0..3``; word j holds eight codes ``i = 0..7``:
-INT4 code i sits at bits ``4 i`` of the little-endian uint32 at slot byte
-``4 j``; INT8 code i is slot byte ``8 j + i``.  With ``r = i & 3`` and
+32 (INT8) bytes per slot.  Slot ``p = 4 gr + t`` (``gr`` in 0..7, ``t`` in
+0..3: the lane order of an mma.sync fragment) holds four words ``j = 0..3``;
+word j holds eight codes ``i = 0..7``: INT4 code i sits at bits ``4 i`` of the
+little-endian uint32 at slot byte ``4 j``; INT8 code i is slot byte
+``8 j + i``.  With ``r = i & 3`` and
 ``e = i >> 2``, code i of word j in slot (gr, t) is the weight at tile
 row / column::
 
@@ -93,8 +94,8 @@ def code_coordinates():
     """Tile (row, col) of every code of a tile, in blob order (mb, h, p, j, i)."""
     mb, h, p, j, i = np.meshgrid(np.arange(8), np.arange(2), np.arange(32), np.arange(4),
                                  np.arange(8), indexing="ij")
-    gr = p % 8
-    t = p // 8
+    gr = p // 4
+    t = p % 4
     r = i & 3
     e = i >> 2
     row = mb * 16 + gr + 8 * (r & 1)

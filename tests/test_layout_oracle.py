@@ -28,11 +28,11 @@ def test_fragment_slots_follow_mma_register_order():
     first = list(zip(row[:8].tolist(), col[:8].tolist()))
     # i = 0..7 -> r = i & 3, e = i >> 2: (row, col)
     assert first == [(0, 0), (8, 0), (0, 2), (8, 2), (0, 1), (8, 1), (0, 3), (8, 3)]
-    # slot p = 9 -> gr = 1, t = 1; word j = 2 -> cols 16 + 8 = 24..27
+    # slot p = 9 -> gr = 2, t = 1; word j = 2 -> cols 16 + 8 = 24..27
     p, j = 9, 2
     idx = (p * 4 + j) * 8
     got = list(zip(row[idx:idx + 8].tolist(), col[idx:idx + 8].tolist()))
-    assert got == [(1, 24), (9, 24), (1, 26), (9, 26), (1, 25), (9, 25), (1, 27), (9, 27)]
+    assert got == [(2, 24), (10, 24), (2, 26), (10, 26), (2, 25), (10, 25), (2, 27), (10, 27)]
 
 
 @pytest.mark.parametrize("N,K,bits,group", [
