@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   const long long t0 = tile_begin(c, a.T, a.G), t1 = tile_begin(c + 1, a.T, a.G);
   const int ntile = (int)(t1 - t0);
   constexpr int kTilesPerStage = tiles_per_stage(BITS);
+  static_assert(kTilesPerStage == 2, "the consumer loop below handles exactly two tiles per stage");
   const int nfill = (ntile + kTilesPerStage - 1) / kTilesPerStage;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full = sbase + (uint32_t)(a.NS * a.stage_bytes);
