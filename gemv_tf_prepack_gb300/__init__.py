@@ -22,7 +22,7 @@ import numpy as np
 
 __all__ = [
     "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "unprepack",
-    "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemm", "device_error",
+    "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemv_noalloc", "gemm", "device_error",
     "header_declarations",
 ]
 
@@ -58,6 +58,7 @@ _SIGNATURES = {
     "tf_gemv_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tf_gemv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
     "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
+    "tf_gemv_noalloc": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
     "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
 }
 
@@ -235,6 +236,20 @@ def gemv(W: Weights, x, y=None, workspace=None, stream=None):
     ws = W.workspace(M) if workspace is None else workspace
     _check(_lib().tf_gemv(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
                           _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "tf_gemv")
+    return y
+
+
+def gemv_noalloc(W: Weights, x, y=None, stream=None):
+    """tf_gemv without a workspace argument (scratch is a fixed array inside libtf).
+
+    For callers that cannot allocate device memory; calls that overlap on the
+    GPU share that scratch and must be ordered on one stream.
+    """
+    _check_x(W, x)
+    M = x.shape[0]
+    y = _out(W, M, y)
+    _check(_lib().tf_gemv_noalloc(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
+                                  _stream(stream)), "tf_gemv_noalloc")
     return y
 
 

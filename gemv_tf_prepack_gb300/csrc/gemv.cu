@@ -531,4 +531,83 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   return launch_gemv<8, 4>(map, a, P.smem, stream);
 }
 
+
+// ===========================================================================
+// tf_gemv_noalloc: tf_gemv with its scratch in a fixed device array.
+//
+// Some callers cannot allocate device memory at the point where they run a
+// layer: code that runs inside another framework's memory pool, plugins
+// handed only input and output pointers, or real-time paths where an
+// allocation may block or fail.  For them the split-K scratch of the GEMV
+// (FP32 partial sums + arrival counters) lives in this file-scope array,
+// which every GPU that loads the library holds until the process exits.
+// Host code must not pass the array's name to a kernel (on the host it is
+// only a stand-in): its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+
+}  // extern "C"
+
+static __device__ __align__(256) unsigned char tf_gemv_scratch[TF_GEMV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of tf_gemv_scratch on the current device (cached per device).
+unsigned char* gemv_scratch_address() {
+  static std::atomic<unsigned char*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  unsigned char* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, tf_gemv_scratch) != cudaSuccess || !addr) return nullptr;
+  cache[dev].store(static_cast<unsigned char*>(addr), std::memory_order_release);
+  return static_cast<unsigned char*>(addr);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                    uint16_t* y, int M, cudaStream_t stream) {
+  Geometry G;
+  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
+  if (rc) return rc;
+  if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
+  if (M > 8) return TF_ERR_UNSUPPORTED;
+  if (!aligned16(x)) return TF_ERR_ALIGNMENT;
+  GemvPlan P;
+  rc = gemv_plan(G, M, &P);
+  if (rc) return rc;
+  if (P.partial_bytes + P.counter_bytes > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
+  unsigned char* scratch = gemv_scratch_address();
+  if (!scratch) return TF_ERR_CUDA;
+  // The arrival counters must start at zero; a call cut short (device error)
+  // could have left them dirty, so clear them on the stream first.
+  unsigned char* counters = scratch + P.partial_bytes;
+  if (cudaMemsetAsync(counters, 0, P.counter_bytes, stream) != cudaSuccess) return TF_ERR_CUDA;
+  CUtensorMap map;
+  rc = encode_x_map(x, M, K, &map);
+  if (rc) return rc;
+  GemvArgs a;
+  a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  a.y = y;
+  a.partials = reinterpret_cast<float4*>(scratch);
+  a.counters = reinterpret_cast<unsigned*>(counters);
+  a.err = device_error_ptr();
+  if (!a.err) return TF_ERR_CUDA;
+  a.T = P.T;
+  a.N = N; a.K = K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
+  a.G = P.G; a.S_max = P.S_max;
+  a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
+  if (bits == 4) {
+    if (G.gpt == 1) return launch_gemv<4, 1>(map, a, P.smem, stream);
+    if (G.gpt == 2) return launch_gemv<4, 2>(map, a, P.smem, stream);
+    return launch_gemv<4, 4>(map, a, P.smem, stream);
+  }
+  if (G.gpt == 1) return launch_gemv<8, 1>(map, a, P.smem, stream);
+  if (G.gpt == 2) return launch_gemv<8, 2>(map, a, P.smem, stream);
+  return launch_gemv<8, 4>(map, a, P.smem, stream);
+}
+
 }  // extern "C"

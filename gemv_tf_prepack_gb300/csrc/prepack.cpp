@@ -144,6 +144,8 @@ const char* tf_status_string(int status) {
     case TF_ERR_BAD_BLOB: return "TF_ERR_BAD_BLOB: blob header or size mismatch";
     case TF_ERR_CUDA: return "TF_ERR_CUDA: CUDA runtime call or launch failed";
     case TF_ERR_DEVICE: return "TF_ERR_DEVICE: a kernel reported an error";
+    case TF_ERR_SCRATCH_LIMIT:
+      return "TF_ERR_SCRATCH_LIMIT: the layer needs more scratch than tf_gemv_noalloc's fixed buffer";
     default: return "unknown tf status";
   }
 }

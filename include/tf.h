@@ -24,8 +24,9 @@
  *    eight codes per word, low nibble first along K; INT8 qweight is uint8
  *    [N, K]; scales uint16 [N, K/g]; zeros uint8 [N, K/g] (0..2^bits-1).
  *  - The caller allocates and owns every buffer.  The library allocates no
- *    memory; its only global state is cached device attributes and one
- *    device-side error word per device.
+ *    memory; its only global state is cached device attributes, one
+ *    device-side error word per device and the fixed scratch array of
+ *    tf_gemv_noalloc.
  *  - Every call returns TF_OK (0) or a negative TF_ERR_* code and never
  *    aborts.  Device calls only enqueue work on the given stream (NULL means
  *    the legacy default stream) and return without synchronising; a
@@ -54,6 +55,7 @@ extern "C" {
 #define TF_ERR_BAD_BLOB (-5)    /* header magic/version/fields do not match */
 #define TF_ERR_CUDA (-6)        /* a CUDA runtime call or a launch failed */
 #define TF_ERR_DEVICE (-7)      /* a kernel reported an error (see tf_device_error) */
+#define TF_ERR_SCRATCH_LIMIT (-8) /* tf_gemv_noalloc: the layer needs more than its fixed scratch */
 
 /* Library version (TF_VERSION). */
 int tf_version(void);
@@ -142,6 +144,31 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
  */
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, cudaStream_t stream);
+
+/*
+ * tf_gemv without a caller-provided workspace, for callers that cannot
+ * allocate device memory where they run the layer (code living inside
+ * another framework's memory pool, plugins that are handed only their input
+ * and output pointers, latency-critical paths where an allocation may block
+ * or fail).  The paper has no counterpart: it is an addition of this
+ * library.  Arguments and results are those of tf_gemv; the split-K scratch
+ * is a fixed device array of TF_GEMV_NOALLOC_SCRATCH_BYTES inside libtf that
+ * every GPU which loads the library keeps until the process exits.  No
+ * cudaMalloc/cudaFree or allocating library routine is called.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing a stream into a CUDA graph.
+ *  - Every call on a device shares the one array and leaves its last
+ *    contents behind; each call first clears the arrival counters on its
+ *    stream.  Calls that overlap on the GPU (other streams, other host
+ *    threads) race on the array: order them on one stream or use tf_gemv.
+ *  - A layer whose scratch would exceed TF_GEMV_NOALLOC_SCRATCH_BYTES is
+ *    rejected with TF_ERR_SCRATCH_LIMIT (every N, K <= 32768 fits on GPUs
+ *    with up to ~200 SMs).
+ */
+#define TF_GEMV_NOALLOC_SCRATCH_BYTES (4u << 20)
+int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                    const uint16_t* x, uint16_t* y, int M, cudaStream_t stream);
 
 /*
  * Read and clear the current device's error word (synchronous).  Kernels
