@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
 //
 // Work split: the T = NB * KT tiles are numbered in blob order and CTA c
 // streams tiles [c*T/G, (c+1)*T/G) — one contiguous byte range, which a
-// shared-memory ring fetches with 1-D bulk copies (two tiles per stage), the
+// shared-memory ring fetches with 1-D bulk copies (four INT4 or two INT8 tiles per stage), the
 // tiles' activation slices x[:, kt*128 : kt*128+128] arriving alongside by
 // 2-D TMA (zero-filled past K).  The warp that hands a stage back last
 // refills it, so no warp is dedicated to (or delayed by) producing.  Warp w
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
 
 constexpr int kGemvConsumers = 8;                  // one warp per 16-row block
 // tiles per ring stage (one bulk copy)
-__host__ __device__ constexpr int tiles_per_stage(int) { return 2; }
+__host__ __device__ constexpr int tiles_per_stage(int bits) { return bits == 4 ? 4 : 2; }
 constexpr int kGemvThreads = 32 * kGemvConsumers;
 constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
 constexpr unsigned kErrGemvWait = 0x600;
@@ -140,20 +140,28 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, int n0, int t, const 
   }
 }
 
-// End of a segment of row block nb: write y directly or go through the
-// workspace and let the last contributor reduce.
-__device__ __forceinline__ void flush_segment(const GemvArgs& a, int c, long long t0, int nb, bool whole,
-                                              int warp, int lane, const float (&v)[4]) {
+// End of a segment of row block nb.  A whole block is written to y at once.
+// A partial one is only stored in the workspace here; it is published (one
+// fence for all of them) and counted at the end of the CTA's range, when no
+// bulk copy of this CTA is in flight any more — a fence issued mid-stream
+// waits behind the stream and delays the whole grid.  Returns true when the
+// segment is pending.
+__device__ __forceinline__ bool end_segment(const GemvArgs& a, int c, long long t0, int nb, bool whole, int warp,
+                                            int lane, const float (&v)[4]) {
   const int gr = lane >> 2, t = lane & 3;
-  const int n0 = nb * kTileN + warp * 16 + gr;
   if (whole) {
-    store_y(a, n0, t, v);
-    return;
+    store_y(a, nb * kTileN + warp * 16 + gr, t, v);
+    return false;
   }
   const int seg = nb - (int)(t0 / a.KT);
   __stcg(a.partials + ((size_t)(c * a.S_max + seg) * 8 + warp) * 32 + lane, make_float4(v[0], v[1], v[2], v[3]));
-  __threadfence();
-  __syncwarp();
+  return true;
+}
+
+// Count this CTA's contribution to row block nb (after the fence); the last
+// contributor adds all partials in CTA order, writes y and resets the counter.
+__device__ __forceinline__ void publish_segment(const GemvArgs& a, int nb, int warp, int lane) {
+  const int gr = lane >> 2, t = lane & 3;
   unsigned old = 0;
   if (lane == 0) old = atomicAdd(a.counters + nb * 8 + warp, 1u);
   old = __shfl_sync(0xFFFFFFFFu, old, 0);
@@ -161,14 +169,28 @@ __device__ __forceinline__ void flush_segment(const GemvArgs& a, int c, long lon
   const int c_first = cta_of_tile(first_tile, a.T, a.G);
   const int c_last = cta_of_tile(first_tile + a.KT - 1, a.T, a.G);
   if (old != (unsigned)(c_last - c_first)) return;
-  __threadfence();
+  fence_acq_rel_gpu();  // acquire: every contributor's partials are visible
+  // Issue the loads of up to sixteen contributors at once, then add them in
+  // CTA order: one L2 round trip per sixteen contributors, same sum every run.
   float s[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int cc = c_first; cc <= c_last; ++cc) {
-    const int sg = nb - (int)(tile_begin(cc, a.T, a.G) / a.KT);
-    const float4 u = __ldcg(a.partials + ((size_t)(cc * a.S_max + sg) * 8 + warp) * 32 + lane);
-    s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
+  for (int c0 = c_first; c0 <= c_last; c0 += 16) {
+    float4 u[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int cc = c0 + j;
+      if (cc <= c_last) {
+        const int sg = nb - (int)(tile_begin(cc, a.T, a.G) / a.KT);
+        u[j] = __ldcg(a.partials + ((size_t)(cc * a.S_max + sg) * 8 + warp) * 32 + lane);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (c0 + j <= c_last) {
+        s[0] += u[j].x; s[1] += u[j].y; s[2] += u[j].z; s[3] += u[j].w;
+      }
+    }
   }
-  store_y(a, n0, t, s);
+  store_y(a, nb * kTileN + warp * 16 + gr, t, s);
   if (lane == 0) a.counters[nb * 8 + warp] = 0u;
 }
 
@@ -183,6 +205,7 @@ struct TileRegs {
 
 struct LaneOffsets {
   int w, s, z, x, gi0, gi1;
+  bool x_on;  // this lane's B-fragment column is a real token (gr < M)
 };
 
 template <int BITS, int GPT>
@@ -194,8 +217,12 @@ __device__ __forceinline__ void load_tile(TileRegs<BITS, GPT>& R, const uint8_t*
   for (int h = 0; h < 2; ++h) {
 #pragma unroll
     for (int v = 0; v < SB / 16; ++v) R.w[h][v] = *reinterpret_cast<const uint4*>(tb + o.w + h * 32 * SB + v * 16);
-    R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
-    R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
+    // Columns of B past M only feed columns of D that are never stored: those
+    // lanes keep whatever their registers hold and skip the shared-memory read.
+    if (o.x_on) {
+      R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
+      R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
+    }
   }
   R.sp[0] = *reinterpret_cast<const uint32_t*>(tb + o.s + o.gi0 * 256);
   R.zp[0] = BITS == 4 ? (uint32_t)tb[o.z + o.gi0 * ZB] : (uint32_t)*reinterpret_cast<const uint16_t*>(tb + o.z + o.gi0 * ZB);
@@ -295,7 +322,6 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   const long long t0 = tile_begin(c, a.T, a.G), t1 = tile_begin(c + 1, a.T, a.G);
   const int ntile = (int)(t1 - t0);
   constexpr int kTilesPerStage = tiles_per_stage(BITS);
-  static_assert(kTilesPerStage == 2, "the consumer loop below handles exactly two tiles per stage");
   const int nfill = (ntile + kTilesPerStage - 1) / kTilesPerStage;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full = sbase + (uint32_t)(a.NS * a.stage_bytes);
@@ -333,59 +359,68 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   o.z = WB + GPT * 256 + (BITS == 4 ? (warp * 8 + gr) : (warp * 8 + gr) * 2);
   o.gi0 = GPT == 1 ? 0 : (16 * t) / a.g;
   o.gi1 = GPT == 1 ? 0 : (64 + 16 * t) / a.g;
-  // Rows of B past M are never stored; those lanes read row M-1 again.
-  o.x = (gr < a.M ? gr : a.M - 1) * 256 + 32 * t;
+  o.x_on = gr < a.M;
+  o.x = (o.x_on ? gr : 0) * 256 + 32 * t;
   const int x_stride = a.M * 256;
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  TileRegs<BITS, GPT> R;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int v = 0; v < 2; ++v) R.x[h][v] = make_uint4(0, 0, 0, 0);
   Segment seg = first_segment(t0, ntile, a.KT);
+  // at most two segments of a contiguous range are partial: its first and its last
+  int pending0 = 0, pending1 = 0, npending = 0;
   int s = 0;
   uint32_t lap = 0;
   for (int f = 0; f < nfill; ++f) {
     if (!mbar_wait(full + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs)) break;
     const int i0 = f * kTilesPerStage;
+    const int n = ntile - i0 < kTilesPerStage ? ntile - i0 : kTilesPerStage;
     const uint8_t* st = smem + s * a.stage_bytes;
     const uint8_t* xs = st + a.x_off;
-    const bool two = i0 + 1 < ntile;
-    TileRegs<BITS, GPT> A, B;
-    load_tile(A, st, xs, o);
-    if (two) load_tile(B, st + a.tile_bytes, xs + x_stride, o);
-    __syncwarp();
-    if (lane == 0) {
-      // the stage is in registers: hand it back; the last warp refills it
-      mbar_arrive(empty + 8 * s);
-      if (atomicAdd(released + s, 1u) == kGemvConsumers - 1) {
-        released[s] = 0;
-        if (f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs))
-          issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true);
+#pragma unroll
+    for (int j = 0; j < kTilesPerStage; ++j) {
+      if (j < n) {
+        load_tile(R, st + j * a.tile_bytes, xs + j * x_stride, o);
+        if (j == n - 1) {
+          // the whole stage has been read: hand it back; the last warp to do
+          // so refills it
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(empty + 8 * s);
+            if (atomicAdd(released + s, 1u) == kGemvConsumers - 1) {
+              released[s] = 0;
+              if (f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs))
+                issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true);
+            }
+          }
+          __syncwarp();
+        }
+        mma_tile(R, acc);
+        if (i0 + j == seg.end) {
+          const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
+                              acc[0][3] + acc[1][3]};
+          if (end_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v)) {
+            if (npending == 0) pending0 = seg.nb; else pending1 = seg.nb;
+            ++npending;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[h][q] = 0.f;
+          next_segment(seg, ntile, a.KT);
+        }
       }
     }
-    __syncwarp();
     if (++s == a.NS) { s = 0; ++lap; }
-
-    mma_tile(A, acc);
-    if (i0 == seg.end) {
-      const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]};
-      flush_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[h][q] = 0.f;
-      next_segment(seg, ntile, a.KT);
-    }
-    if (two) {
-      mma_tile(B, acc);
-      if (i0 + 1 == seg.end) {
-        const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
-                            acc[0][3] + acc[1][3]};
-        flush_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[h][q] = 0.f;
-        next_segment(seg, ntile, a.KT);
-      }
-    }
+  }
+  if (npending > 0) {
+    fence_acq_rel_gpu();  // release: this lane's partials before any count below
+    __syncwarp();
+    publish_segment(a, pending0, warp, lane);
+    if (npending > 1) publish_segment(a, pending1, warp, lane);
   }
 }
 
@@ -397,7 +432,7 @@ struct GemvPlan {
   size_t smem, partial_bytes, counter_bytes;
 };
 
-constexpr int kGemvSmemBudget = 100 * 1024;  // ring bytes per CTA; two CTAs share an SM
+constexpr int kGemvSmemBudget = 110 * 1024;  // ring bytes per CTA; two CTAs share an SM
 constexpr int kGemvSmemMax = 113 * 1024;
 
 inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {

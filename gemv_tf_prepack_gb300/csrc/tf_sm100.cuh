@@ -96,6 +96,10 @@ __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Release/acquire fence at GPU scope (lighter than the sequentially
+// consistent fence __threadfence issues).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch (no-ops unless the launch enables it)
 
