@@ -8,9 +8,9 @@
 //                tile is contiguous and carries its own scales and zeros)
 //                and the matching activation slabs (2-D TMA, 128-byte
 //                swizzle) into shared-memory rings;
-//   warps 6..13  unpack + dequantise one 16-row block each into the UMMA
-//                K-major 128-byte-swizzled layout (bit-exact
-//                bf16_rne((q - z) * s)), 64 K-columns at a time;
+//   warps 6..21  unpack + dequantise one (16-row block, 64-column slab) of
+//                each tile into the UMMA K-major 128-byte-swizzled layout
+//                (bit-exact bf16_rne((q - z) * s));
 //   warp 1       issues tcgen05.mma (M = 128 weight rows, N = BN tokens,
 //                K = 16) from one thread, accumulating in tensor memory;
 //                two accumulators let the epilogue of one tile overlap the
@@ -36,8 +36,8 @@ namespace tf {
 
 namespace {
 
-constexpr int kThreads = 448;        // 14 warps
-constexpr int kDequantWarp0 = 6;     // warps 6..13
+constexpr int kThreads = 704;        // 22 warps
+constexpr int kDequantWarp0 = 6;     // warps 6..21: (row block, slab) pairs
 constexpr int kEpilogueWarp0 = 2;    // warps 2..5
 constexpr int kSlabBytesW = 128 * 128;  // 128 rows x 64 BF16
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.P; ++i) {
       mbar_init(B.full_p + 8 * i, 1);
-      mbar_init(B.empty_p + 8 * i, 8);
+      mbar_init(B.empty_p + 8 * i, 16);  // every dequant warp reads the tile
     }
     for (int i = 0; i < a.OPS; ++i) {
       mbar_init(B.full_op + 8 * i, 1 + 8);  // producer (with tx) + 8 dequant warps
@@ -215,7 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     // ---------------------------------------------------------------- dequant
-    const int mb = warp - kDequantWarp0;  // 16-row block of every tile
+    // Warp (mb, h): 16-row block mb of the 64-column slab h of every tile, so
+    // the two slabs of a tile are dequantised in parallel.
+    const int dw = warp - kDequantWarp0;
+    const int mb = dw & 7, h = dw >> 3;
     const int gr = lane >> 2, t = lane & 3;  // lane reads slot p = lane (conflict-free)
     constexpr int WB = kTileN * kTileK * BITS / 8;
     constexpr int SB = BITS == 4 ? 16 : 32;
@@ -232,61 +235,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         dst[e][cc] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
       }
     }
-    int ps = 0, os = 0;
-    uint32_t pph = 0, oph = 0;
+    const int gi = GPT == 1 ? 0 : (h * 64 + 16 * t) / a.g;
+    const int s_off = WB + gi * 256 + (mb * 8 + gr) * 4;
+    const int z_off = WB + GPT * 256 + gi * ZB + (BITS == 4 ? (mb * 8 + gr) : (mb * 8 + gr) * 2);
+    const int w_off = ((mb * 2 + h) * 32 + lane) * SB;
+    int ps = 0;
+    uint32_t pph = 0;
+    unsigned slab = (unsigned)h;  // this warp's slabs are h, h + 2, h + 4, ... of the CTA's stream
     bool ok = true;
     for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
       for (int kt = 0; kt < a.KT && ok; ++kt) {
         ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, kTimeoutNs);
         if (!ok) break;
         const uint8_t* pk = smem + (size_t)ps * a.tile_bytes;
+        const uint32_t sp = *reinterpret_cast<const uint32_t*>(pk + s_off);
+        uint32_t lo[8], hi[8];
+        if (BITS == 4) {
+          const MetaW4 m = meta_w4(sp, pk[z_off]);
+          const uint4 v = *reinterpret_cast<const uint4*>(pk + w_off);
+          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int gi = GPT == 1 ? 0 : (h * 64 + 16 * t) / a.g;
-          const uint32_t sp = *reinterpret_cast<const uint32_t*>(pk + WB + gi * 256 + (mb * 8 + gr) * 4);
-          const uint8_t* slot = pk + ((mb * 2 + h) * 32 + lane) * SB;
-          uint32_t lo[8], hi[8];
-          if (BITS == 4) {
-            const MetaW4 m = meta_w4(sp, pk[WB + GPT * 256 + gi * ZB + mb * 8 + gr]);
-            const uint4 v = *reinterpret_cast<const uint4*>(slot);
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t f[4];
-              dequant_w4(words[j], m, f);
-              lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
-              hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
-            }
-          } else {
-            const uint32_t zp = *reinterpret_cast<const uint16_t*>(pk + WB + GPT * 256 + gi * ZB + (mb * 8 + gr) * 2);
-            const MetaW8 m = meta_w8(sp, zp);
-            const uint4 v0 = reinterpret_cast<const uint4*>(slot)[0];
-            const uint4 v1 = reinterpret_cast<const uint4*>(slot)[1];
-            const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t f[4];
-              dequant_w8(words[2 * j], words[2 * j + 1], m, f);
-              lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
-              hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
-            }
+          for (int j = 0; j < 4; ++j) {
+            uint32_t f[4];
+            dequant_w4(words[j], m, f);
+            lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
+            hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
           }
-          ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, kTimeoutNs);
-          if (!ok) break;
-          uint8_t* wsl = smem + a.off_op + (size_t)os * op_stage_bytes;
-          *reinterpret_cast<uint4*>(wsl + dst[0][0]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          *reinterpret_cast<uint4*>(wsl + dst[0][1]) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-          *reinterpret_cast<uint4*>(wsl + dst[1][0]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(wsl + dst[1][1]) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-          fence_async_shared();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(B.full_op + 8 * os);
-          if (++os == a.OPS) { os = 0; oph ^= 1; }
+        } else {
+          const MetaW8 m = meta_w8(sp, *reinterpret_cast<const uint16_t*>(pk + z_off));
+          const uint4 v0 = reinterpret_cast<const uint4*>(pk + w_off)[0];
+          const uint4 v1 = reinterpret_cast<const uint4*>(pk + w_off)[1];
+          const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t f[4];
+            dequant_w8(words[2 * j], words[2 * j + 1], m, f);
+            lo[2 * j] = f[0]; lo[2 * j + 1] = f[2];
+            hi[2 * j] = f[1]; hi[2 * j + 1] = f[3];
+          }
         }
-        if (!ok) break;
+        // the packed tile is in registers: hand it back
         __syncwarp();
         if (lane == 0) mbar_arrive(B.empty_p + 8 * ps);
         if (++ps == a.P) { ps = 0; pph ^= 1; }
+        const unsigned os = slab % (unsigned)a.OPS;
+        const uint32_t oph = (slab / (unsigned)a.OPS) & 1u;
+        ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, kTimeoutNs);
+        if (!ok) break;
+        uint8_t* wsl = smem + a.off_op + (size_t)os * op_stage_bytes;
+        *reinterpret_cast<uint4*>(wsl + dst[0][0]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(wsl + dst[0][1]) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        *reinterpret_cast<uint4*>(wsl + dst[1][0]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(wsl + dst[1][1]) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.full_op + 8 * os);
+        slab += 2;
       }
     }
   }
