@@ -99,3 +99,15 @@ def test_gemm_deterministic():
     a = to_host_bits(tf.gemm(W, x))
     b = to_host_bits(tf.gemm(W, x))
     np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("N,K,bits,group", [(512, 1024, 4, 128), (256, 768, 8, 0), (384 + 128, 640, 4, 64),
+                                            (1000, 1016, 4, 0), (256, 512, 4, 32)])
+@pytest.mark.parametrize("M", [256, 300, 640, 1000])
+def test_gemm_even_blocks(N, K, bits, group, M):
+    """Even numbers of 128-row blocks with several ragged 256-token tiles."""
+    qw, W = layer(N, K, bits, group, 37)
+    xb = synth.make_activations(M, K, 37, outliers=True)
+    y = to_host_bits(tf.gemm(W, to_dev_bf16(xb)))
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
+    check_close(y, ref, f"gemm {N}x{K} w{bits} g{group} M={M}")
