@@ -376,8 +376,8 @@ def run_ours(args, rank, world):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-            "traffic": recorded_traffic("gemv_kernel", GEMV_SOURCES),
-            "kernel": "gemv_kernel<4,1>", "algorithmic_bytes_per_launch": round(per_launch_bytes),
+            "traffic": recorded_traffic("gemv_slab_kernel", GEMV_SOURCES),
+            "kernel": "gemv_slab_kernel<4,1>", "algorithmic_bytes_per_launch": round(per_launch_bytes),
             "kernel_us_per_launch": round(kernel_ms * 1e3, 3),
             "isolated_launch_us": iso_us,
         },
@@ -475,6 +475,40 @@ def run_reference(args, rank, world):
     }
 
 
+PROFILE_CASES = {
+    # name: (launch kind, M, [(N, K, seed)], outliers)
+    "decode": ("gemv", 1, DECODE, False),
+    "prefill": ("gemm", PREFILL_M, PREFILL, True),
+    "large": ("gemv", 1, [(32768, 32768, 12)], False),
+    "large_gemm": ("gemm", 4096, [(32768, 8192, 10)], False),
+}
+
+
+def run_profile(case: str, reps: int):
+    """A short, untimed run of one workload's launches, for profiler captures.
+
+    Every launch runs `reps` times, in the order of the benchmark's step, on
+    one weight copy; nothing is timed or printed but a one-line summary.
+    """
+    import torch
+
+    import gemv_tf_prepack_gb300 as tf
+    from gemv_tf_prepack_gb300 import synth
+
+    kind, M, shapes, outliers = PROFILE_CASES[case]
+    torch.cuda.set_device(0)
+    layers = build_layers(torch, tf, synth, shapes, M, outliers, 1)
+    fn = tf.gemv if kind == "gemv" else tf.gemm
+    for _ in range(reps):
+        for L in layers:
+            fn(L["Ws"][0], L["xs"][0], L["ys"][0])
+    torch.cuda.synchronize()
+    err = tf.device_error()
+    print(f"profile {case}: {reps} x {len(layers)} {kind} launches, device error {err}")
+    if err:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -483,9 +517,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                    help="run one workload's launches a few times, untimed (for ncu captures)")
+    ap.add_argument("--profile-reps", type=int, default=2)
     args = ap.parse_args()
     if args.oracle_sample:
         print(json.dumps(oracle_sample()))
+        return
+    if args.profile:
+        run_profile(args.profile, args.profile_reps)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -4,8 +4,8 @@
 // *once* into on-chip memory and the BF16 result is reused for the tile's
 // matrix operations.  Here, per CTA output tile of 128 weight rows x BN
 // tokens (BN <= 256):
-//   warp 0       streams pre-tiled weight tiles (one 1-D bulk copy each: a
-//                tile is contiguous and carries its own scales and zeros)
+//   warp 0       streams pre-tiled weight tiles (eight 1-D bulk copies, one
+//                per 16-row unit, each carrying its own scales and zeros)
 //                and the matching activation slabs (2-D TMA, 128-byte
 //                swizzle) into shared-memory rings;
 //   warps 6..21  unpack + dequantise one (16-row block, 64-column slab) of
@@ -52,10 +52,10 @@ enum : unsigned {
 };
 
 struct GemmArgs {
-  const uint8_t* tiles;
+  const uint8_t* units;
   uint16_t* y;
   unsigned* err;              // device error word
-  int N, K, M, KT, g, tile_bytes;
+  int N, K, M, KT, g, tile_bytes;  // tile_bytes: one packed tile (eight units) in shared memory
   int MT, BN, ntiles;
   int P, OPS;                 // stages of the packed ring and of the operand ring
   int off_op, off_bar;        // byte offsets in the 1024-aligned dynamic smem
@@ -118,28 +118,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int ps = 0, os = 0;
-      uint32_t pph = 0, oph = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-        const int nb = tile / a.MT, mt = tile - nb * a.MT;
-        const uint8_t* src = a.tiles + (size_t)nb * a.KT * a.tile_bytes;
-        for (int kt = 0; kt < a.KT && ok; ++kt) {
-          ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
-          if (!ok) break;
-          mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
-          bulk_load(sbase + (uint32_t)ps * a.tile_bytes, src + (size_t)kt * a.tile_bytes, (uint32_t)a.tile_bytes,
+    // Lane i < 8 copies unit i (rows 16i .. 16i + 15) of each tile; lane 0
+    // arms the barriers and loads the activation slabs.
+    constexpr int UB = unit_bytes_gpu(BITS, GPT);
+    int ps = 0, os = 0;
+    uint32_t pph = 0, oph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+      const int nb = tile / a.MT, mt = tile - nb * a.MT;
+      const uint8_t* src = a.units + ((size_t)(nb * kSlabsPerTile + (lane & 7)) * a.KT) * UB;
+      for (int kt = 0; kt < a.KT && ok; ++kt) {
+        ok = mbar_wait_warp(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
+        __syncwarp();
+        if (lane < kSlabsPerTile)
+          bulk_load(sbase + (uint32_t)(ps * a.tile_bytes + lane * UB), src + (size_t)kt * UB, (uint32_t)UB,
                     B.full_p + 8 * ps);
-          if (++ps == a.P) { ps = 0; pph ^= 1; }
-          for (int h = 0; h < 2; ++h) {
-            ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
-            if (!ok) break;
+        if (++ps == a.P) { ps = 0; pph ^= 1; }
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait_warp(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
+          if (!ok) break;
+          if (lane == 0) {
             mbar_arrive_expect_tx(B.full_op + 8 * os, x_slab_bytes);
             tma_load_2d(sbase + a.off_op + (uint32_t)os * op_stage_bytes + kSlabBytesW, &tmx,
                         kt * kTileK + h * 64, mt * a.BN, B.full_op + 8 * os);
-            if (++os == a.OPS) { os = 0; oph ^= 1; }
           }
+          if (++os == a.OPS) { os = 0; oph ^= 1; }
         }
       }
     }
@@ -215,14 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     // ---------------------------------------------------------------- dequant
-    // Warp (mb, h): 16-row block mb of the 64-column slab h of every tile, so
-    // the two slabs of a tile are dequantised in parallel.
+    // Warp (mb, h): unit mb (rows 16 mb .. 16 mb + 15) and 64-column slab h
+    // of every tile, so the two slabs of a tile are dequantised in parallel.
     const int dw = warp - kDequantWarp0;
     const int mb = dw & 7, h = dw >> 3;
     const int gr = lane >> 2, t = lane & 3;  // lane reads slot p = lane (conflict-free)
-    constexpr int WB = kTileN * kTileK * BITS / 8;
+    constexpr int UB = unit_bytes_gpu(BITS, GPT);
     constexpr int SB = BITS == 4 ? 16 : 32;
-    constexpr int ZB = BITS == 4 ? 64 : 128;
     const int r0 = mb * 16 + gr;  // rows r0 and r0 + 8 of the 128-row slab
     // byte offsets of this lane's two 16-byte chunks in rows r0, r0 + 8
     uint32_t dst[2][2];
@@ -236,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
     const int gi = GPT == 1 ? 0 : (h * 64 + 16 * t) / a.g;
-    const int s_off = WB + gi * 256 + (mb * 8 + gr) * 4;
-    const int z_off = WB + GPT * 256 + gi * ZB + (BITS == 4 ? (mb * 8 + gr) : (mb * 8 + gr) * 2);
-    const int w_off = ((mb * 2 + h) * 32 + lane) * SB;
+    const int s_off = mb * UB + unit_scale_offset(BITS, gi, gr);
+    const int z_off = mb * UB + unit_zero_offset(BITS, GPT, gi, gr);
+    const int w_off = mb * UB + (h * 32 + lane) * SB;
     int ps = 0;
     uint32_t pph = 0;
     unsigned slab = (unsigned)h;  // this warp's slabs are h, h + 2, h + 4, ... of the CTA's stream
@@ -314,7 +318,7 @@ struct GemmPlan {
 
 int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
   GemmArgs& a = P->a;
-  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
+  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = kSlabsPerTile * G.unit_bytes;
   a.BN = M >= 256 ? 256 : (M + 15) / 16 * 16;
   a.MT = (M + a.BN - 1) / a.BN;
   a.ntiles = G.NB * a.MT;
@@ -322,7 +326,7 @@ int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
   a.OPS = 0;
   for (int ops = 4; ops >= 2 && a.OPS == 0; --ops)
     for (int p = 4; p >= 2; --p) {
-      const int off_op = (p * G.tile_bytes + 1023) / 1024 * 1024;
+      const int off_op = (p * a.tile_bytes + 1023) / 1024 * 1024;
       const int off_bar = off_op + ops * op_stage;
       const size_t smem = 1024 + off_bar + 256;
       if (smem <= (size_t)kMaxSmem) {
@@ -371,7 +375,7 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   GemmPlan P;
   rc = gemm_plan(G, M, &P);
   if (rc) return rc;
-  P.a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   P.a.y = y;
   P.a.err = device_error_ptr();
   if (!P.a.err) return TF_ERR_CUDA;

@@ -4,11 +4,19 @@
 // co-design").  The pages' point is that a quantised GEMV, memory-bound at
 // full precision, turns compute-bound once unpack and dequant are added, and
 // that the weight stream must be spread over the whole array.  The GB300
-// version: every SM streams one contiguous run of pre-tiled bytes (the
-// blob's tile order makes each CTA's share a single address range), each
-// lane unpacks and dequantises its codes in registers, and the dequantised
-// BF16 fragments go straight into mma.sync so that the tensor cores do the
+// version: every SM streams contiguous runs of pre-tiled units, each lane
+// unpacks and dequantises its codes in registers, and the dequantised BF16
+// fragments go straight into mma.sync so that the tensor cores do the
 // multiply-accumulate instead of CUDA-core FMAs.
+//
+// Two kernels share that inner step (one 16-row x 128-column unit per warp):
+//  * slab GEMV, for layers with at least as many 16-row slabs as SMs: each
+//    CTA owns whole slabs over all of K, its eight warps split K, and a
+//    slab's eight partial sums meet in shared memory.  No CTA waits on
+//    another, so a layer ends as soon as its last slab is done.
+//  * tile GEMV, for the rest (few rows or short K): K is split across CTAs
+//    too; a 128-row block shared by several CTAs is summed by the last of
+//    them, in a fixed order, from FP32 partials in a workspace.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -23,29 +31,28 @@ namespace tf {
 namespace {
 
 // ===========================================================================
-// tf_dequant: one CTA per tile, one thread per (row block, quad, slot).
+// tf_dequant: one CTA per 128 x 128 tile, one thread per (slab, K half, slot).
 
 template <int BITS, int GPT>
-__global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict__ tiles, int N, int K,
-                                                      int KT, int g, int tile_bytes,
-                                                      uint16_t* __restrict__ w) {
+__global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict__ units, int N, int K,
+                                                      int KT, int g, uint16_t* __restrict__ w) {
+  constexpr int UB = unit_bytes_gpu(BITS, GPT);
+  constexpr int SB = BITS == 4 ? 16 : 32;
   const int tile = blockIdx.x;
   const int nb = tile / KT, kt = tile - nb * KT;
   const int mb = threadIdx.x >> 6;
   const int h = (threadIdx.x >> 5) & 1;
   const int p = threadIdx.x & 31;
   const int gr = p >> 2, t = p & 3;
-  constexpr int WB = kTileN * kTileK * BITS / 8;
-  constexpr int SB = BITS == 4 ? 16 : 32;
-  constexpr int ZB = BITS == 4 ? 64 : 128;
-  const uint8_t* tb = tiles + (size_t)tile * tile_bytes;
+  const uint8_t* ub = units + ((size_t)(nb * kSlabsPerTile + mb) * KT + kt) * UB;
   const int gi = GPT == 1 ? 0 : (h * 64 + 16 * t) / g;
-  const uint32_t sp = *reinterpret_cast<const uint32_t*>(tb + WB + gi * 256 + (mb * 8 + gr) * 4);
-  const uint8_t* slot = tb + ((mb * 2 + h) * 32 + p) * SB;
+  const uint32_t sp = *reinterpret_cast<const uint32_t*>(ub + unit_scale_offset(BITS, gi, gr));
+  const uint8_t* slot = ub + (h * 32 + p) * SB;
+  const uint8_t* zp = ub + unit_zero_offset(BITS, GPT, gi, gr);
 
-  uint32_t lo[8], hi[8];  // rows gr and gr + 8 of this block, 16 columns each
+  uint32_t lo[8], hi[8];  // rows gr and gr + 8 of this slab, 16 columns each
   if (BITS == 4) {
-    const MetaW4 m = meta_w4(sp, tb[WB + GPT * 256 + gi * ZB + mb * 8 + gr]);
+    const MetaW4 m = meta_w4(sp, *zp);
     const uint4 v = *reinterpret_cast<const uint4*>(slot);
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -56,8 +63,7 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
       hi[2 * j] = a[1]; hi[2 * j + 1] = a[3];
     }
   } else {
-    const uint32_t zp = *reinterpret_cast<const uint16_t*>(tb + WB + GPT * 256 + gi * ZB + (mb * 8 + gr) * 2);
-    const MetaW8 m = meta_w8(sp, zp);
+    const MetaW8 m = meta_w8(sp, *reinterpret_cast<const uint16_t*>(zp));
     const uint4 v0 = reinterpret_cast<const uint4*>(slot)[0];
     const uint4 v1 = reinterpret_cast<const uint4*>(slot)[1];
     const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -69,7 +75,7 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
       hi[2 * j] = a[1]; hi[2 * j + 1] = a[3];
     }
   }
-  const int n0 = nb * kTileN + mb * 16 + gr;
+  const int n0 = nb * kTileN + mb * kSlabN + gr;
   const int k0 = kt * kTileK + h * 64 + 16 * t;
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
@@ -83,41 +89,166 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
 }
 
 // ===========================================================================
-// tf_gemv
+// GEMV: the per-warp unit step shared by both kernels.
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = 32 * kGemvWarps;
+constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
+constexpr uint64_t kGemvDrainNs = 200000000ull;  // bounded wait for copies still in flight after an error
+constexpr unsigned kErrGemvWait = 0x600;
+
+// Registers of one unit for one lane: its weight slot in both K halves, the
+// activation fragments and the unit's scale / zero words.
+template <int BITS, int GPT>
+struct UnitRegs {
+  uint4 w[2][BITS == 4 ? 1 : 2];
+  uint4 x[2][2];
+  uint32_t sp[GPT == 1 ? 1 : 2], zp[GPT == 1 ? 1 : 2];
+};
+
+// Unit-relative byte offsets of one lane's operands.
+struct LaneOffsets {
+  int w, s0, s1, z0, z1, x;
+  bool x_on;  // this lane's B-fragment column is a real token (gr < M)
+};
+
+template <int BITS, int GPT>
+__device__ __forceinline__ LaneOffsets lane_offsets(int lane, int g, int M) {
+  constexpr int SB = BITS == 4 ? 16 : 32;
+  const int gr = lane >> 2, t = lane & 3;
+  const int gi0 = GPT == 1 ? 0 : (16 * t) / g;         // group of this lane's columns in K half 0
+  const int gi1 = GPT == 1 ? 0 : (64 + 16 * t) / g;    // ... and in K half 1
+  LaneOffsets o;
+  o.w = lane * SB;  // slot p = 4 gr + t = lane
+  o.s0 = unit_scale_offset(BITS, gi0, gr);
+  o.s1 = unit_scale_offset(BITS, gi1, gr);
+  o.z0 = unit_zero_offset(BITS, GPT, gi0, gr);
+  o.z1 = unit_zero_offset(BITS, GPT, gi1, gr);
+  o.x_on = gr < M;
+  o.x = (o.x_on ? gr : 0) * 256 + 32 * t;
+  return o;
+}
+
+// ub: the unit in shared memory; xb: its activation slice x[0..M)[128 columns].
+template <int BITS, int GPT>
+__device__ __forceinline__ void load_unit(UnitRegs<BITS, GPT>& R, const uint8_t* ub, const uint8_t* xb,
+                                          const LaneOffsets& o) {
+  constexpr int SB = BITS == 4 ? 16 : 32;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int v = 0; v < SB / 16; ++v) R.w[h][v] = *reinterpret_cast<const uint4*>(ub + o.w + h * 32 * SB + v * 16);
+    // Columns of B past M only feed columns of D that are never stored: those
+    // lanes keep whatever their registers hold and skip the shared-memory read.
+    if (o.x_on) {
+      R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
+      R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
+    }
+  }
+  R.sp[0] = *reinterpret_cast<const uint32_t*>(ub + o.s0);
+  R.zp[0] = BITS == 4 ? (uint32_t)ub[o.z0] : (uint32_t)*reinterpret_cast<const uint16_t*>(ub + o.z0);
+  if (GPT > 1) {
+    R.sp[GPT == 1 ? 0 : 1] = *reinterpret_cast<const uint32_t*>(ub + o.s1);
+    R.zp[GPT == 1 ? 0 : 1] = BITS == 4 ? (uint32_t)ub[o.z1] : (uint32_t)*reinterpret_cast<const uint16_t*>(ub + o.z1);
+  }
+}
+
+template <int BITS, int GPT>
+__device__ __forceinline__ void clear_x(UnitRegs<BITS, GPT>& R) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int v = 0; v < 2; ++v) R.x[h][v] = make_uint4(0, 0, 0, 0);
+}
+
+// Unpack, dequantise (bit-exact BF16) and multiply-accumulate one unit.
+template <int BITS, int GPT>
+__device__ __forceinline__ void mma_unit(const UnitRegs<BITS, GPT>& R, float (&acc)[2][4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int mi = GPT == 1 ? 0 : h;
+    const uint32_t xs[8] = {R.x[h][0].x, R.x[h][0].y, R.x[h][0].z, R.x[h][0].w,
+                            R.x[h][1].x, R.x[h][1].y, R.x[h][1].z, R.x[h][1].w};
+    if (BITS == 4) {
+      const MetaW4 m = meta_w4(R.sp[mi], R.zp[mi]);
+      const uint32_t words[4] = {R.w[h][0].x, R.w[h][0].y, R.w[h][0].z, R.w[h][0].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t af[4];
+        dequant_w4(words[j], m, af);
+        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
+      }
+    } else {
+      const MetaW8 m = meta_w8(R.sp[mi], R.zp[mi]);
+      const uint4 v0 = R.w[h][0], v1 = R.w[h][BITS == 4 ? 0 : 1];
+      const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t af[4];
+        dequant_w8(words[2 * j], words[2 * j + 1], m, af);
+        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
+      }
+    }
+  }
+}
+
+// v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1.
+__device__ __forceinline__ void store_y(uint16_t* y, int N, int M, int n0, int t, const float (&v)[4]) {
+  const int m0 = 2 * t, m1 = 2 * t + 1, n1 = n0 + 8;
+  if (n0 < N) {
+    if (m0 < M) y[(size_t)m0 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
+    if (m1 < M) y[(size_t)m1 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
+  }
+  if (n1 < N) {
+    if (m0 < M) y[(size_t)m0 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2]));
+    if (m1 < M) y[(size_t)m1 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[3]));
+  }
+}
+
+__device__ __forceinline__ uint8_t* align128(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
+}
+
+// Wait on a ring barrier with every lane; the result is the same for the
+// whole warp (a lane that gave up makes the warp give up).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_warp(bar, parity, err, kErrGemvWait, kGemvTimeoutNs);
+}
+
+// ===========================================================================
+// tile GEMV (split-K across CTAs)
 //
-// Work split: the T = NB * KT tiles are numbered in blob order and CTA c
-// streams tiles [c*T/G, (c+1)*T/G) — one contiguous byte range, which a
-// shared-memory ring fetches with 1-D bulk copies (four INT4 or two INT8 tiles per stage), the
-// tiles' activation slices x[:, kt*128 : kt*128+128] arriving alongside by
-// 2-D TMA (zero-filled past K).  The warp that hands a stage back last
-// refills it, so no warp is dedicated to (or delayed by) producing.  Warp w
-// of the CTA owns row block w (16 rows) of every tile, so no intra-CTA
-// reduction is needed.  A
+// Work split: the T = NB * KT tiles (eight units: the eight slabs of a
+// 128-row block at one kt) are numbered n-block major and CTA c streams tiles
+// [c*T/G, (c+1)*T/G).  A shared-memory ring holds four INT4 or two INT8 tiles
+// per stage (one bulk copy per unit, issued by the lanes of one warp); the
+// tiles' activation slices x[:, kt*128 : kt*128+128] arrive alongside by 2-D
+// TMA (zero-filled past K).  The warp that hands a stage back last refills
+// it, so no warp is dedicated to (or delayed by) producing.  Warp w of the
+// CTA owns slab w of every tile, so no intra-CTA reduction is needed.  A
 // CTA's range covers whole or partial 128-row blocks ("segments"); a whole
 // block is written straight to y, a partial one is stored as FP32 fragments
 // in the workspace and the last of the block's contributors (arrival counter
-// per row block) adds them in CTA order — a fixed order, so the result does
-// not depend on arrival order.
+// per slab) adds them in CTA order — a fixed order, so the result does not
+// depend on arrival order.
 //
-// The kernel is launched with programmatic dependent launch: the weight
-// stream (static data) starts before the previous kernel on the stream has
+// Both GEMV kernels use programmatic dependent launch: the weight stream
+// (static data) starts before the previous kernel on the stream has
 // finished; activations, y and the workspace are touched only after it has.
 
-constexpr int kGemvConsumers = 8;                  // one warp per 16-row block
-// tiles per ring stage (one bulk copy)
+// tiles per ring stage of the tile GEMV
 __host__ __device__ constexpr int tiles_per_stage(int bits) { return bits == 4 ? 4 : 2; }
-constexpr int kGemvThreads = 32 * kGemvConsumers;
-constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
-constexpr unsigned kErrGemvWait = 0x600;
+static_assert(tiles_per_stage(4) * kSlabsPerTile <= 32 && tiles_per_stage(8) * kSlabsPerTile <= 32,
+              "one lane issues the bulk copy of one unit of a stage");
 
 struct GemvArgs {
-  const uint8_t* tiles;
+  const uint8_t* units;
   uint16_t* y;
   float4* partials;    // [G][S_max][8 warps][32 lanes]
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
   unsigned* err;
   long long T;
-  int N, K, M, KT, g, tile_bytes, G, S_max;
+  int N, K, M, KT, g, G, S_max;
   int NS, stage_bytes, x_off;  // shared-memory ring: stages, bytes per stage, x slice offset
 };
 
@@ -126,18 +257,6 @@ __device__ __forceinline__ long long tile_begin(long long c, long long T, int G)
 // CTA whose range holds tile x.
 __device__ __forceinline__ int cta_of_tile(long long x, long long T, int G) {
   return (int)(((x + 1) * G - 1) / T);
-}
-
-__device__ __forceinline__ void store_y(const GemvArgs& a, int n0, int t, const float (&v)[4]) {
-  const int m0 = 2 * t, m1 = 2 * t + 1, n1 = n0 + 8;
-  if (n0 < a.N) {
-    if (m0 < a.M) a.y[(size_t)m0 * a.N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
-    if (m1 < a.M) a.y[(size_t)m1 * a.N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
-  }
-  if (n1 < a.N) {
-    if (m0 < a.M) a.y[(size_t)m0 * a.N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2]));
-    if (m1 < a.M) a.y[(size_t)m1 * a.N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[3]));
-  }
 }
 
 // End of a segment of row block nb.  A whole block is written to y at once.
@@ -150,7 +269,7 @@ __device__ __forceinline__ bool end_segment(const GemvArgs& a, int c, long long 
                                             int lane, const float (&v)[4]) {
   const int gr = lane >> 2, t = lane & 3;
   if (whole) {
-    store_y(a, nb * kTileN + warp * 16 + gr, t, v);
+    store_y(a.y, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, v);
     return false;
   }
   const int seg = nb - (int)(t0 / a.KT);
@@ -190,82 +309,12 @@ __device__ __forceinline__ void publish_segment(const GemvArgs& a, int nb, int w
       }
     }
   }
-  store_y(a, nb * kTileN + warp * 16 + gr, t, s);
+  store_y(a.y, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, s);
   if (lane == 0) a.counters[nb * 8 + warp] = 0u;
 }
 
-// Registers of one tile for one consumer lane: its weight slot in both K
-// quads, the activation fragments and the tile's scale / zero words.
-template <int BITS, int GPT>
-struct TileRegs {
-  uint4 w[2][BITS == 4 ? 1 : 2];
-  uint4 x[2][2];
-  uint32_t sp[GPT == 1 ? 1 : 2], zp[GPT == 1 ? 1 : 2];
-};
-
-struct LaneOffsets {
-  int w, s, z, x, gi0, gi1;
-  bool x_on;  // this lane's B-fragment column is a real token (gr < M)
-};
-
-template <int BITS, int GPT>
-__device__ __forceinline__ void load_tile(TileRegs<BITS, GPT>& R, const uint8_t* tb, const uint8_t* xb,
-                                          const LaneOffsets& o) {
-  constexpr int SB = BITS == 4 ? 16 : 32;
-  constexpr int ZB = BITS == 4 ? 64 : 128;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int v = 0; v < SB / 16; ++v) R.w[h][v] = *reinterpret_cast<const uint4*>(tb + o.w + h * 32 * SB + v * 16);
-    // Columns of B past M only feed columns of D that are never stored: those
-    // lanes keep whatever their registers hold and skip the shared-memory read.
-    if (o.x_on) {
-      R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
-      R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
-    }
-  }
-  R.sp[0] = *reinterpret_cast<const uint32_t*>(tb + o.s + o.gi0 * 256);
-  R.zp[0] = BITS == 4 ? (uint32_t)tb[o.z + o.gi0 * ZB] : (uint32_t)*reinterpret_cast<const uint16_t*>(tb + o.z + o.gi0 * ZB);
-  if (GPT > 1) {
-    R.sp[GPT == 1 ? 0 : 1] = *reinterpret_cast<const uint32_t*>(tb + o.s + o.gi1 * 256);
-    R.zp[GPT == 1 ? 0 : 1] = BITS == 4 ? (uint32_t)tb[o.z + o.gi1 * ZB]
-                                        : (uint32_t)*reinterpret_cast<const uint16_t*>(tb + o.z + o.gi1 * ZB);
-  }
-}
-
-// Unpack, dequantise (bit-exact BF16) and multiply-accumulate one tile.
-template <int BITS, int GPT>
-__device__ __forceinline__ void mma_tile(const TileRegs<BITS, GPT>& R, float (&acc)[2][4]) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int mi = GPT == 1 ? 0 : h;
-    const uint32_t xs[8] = {R.x[h][0].x, R.x[h][0].y, R.x[h][0].z, R.x[h][0].w,
-                            R.x[h][1].x, R.x[h][1].y, R.x[h][1].z, R.x[h][1].w};
-    if (BITS == 4) {
-      const MetaW4 m = meta_w4(R.sp[mi], R.zp[mi]);
-      const uint32_t words[4] = {R.w[h][0].x, R.w[h][0].y, R.w[h][0].z, R.w[h][0].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t af[4];
-        dequant_w4(words[j], m, af);
-        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
-      }
-    } else {
-      const MetaW8 m = meta_w8(R.sp[mi], R.zp[mi]);
-      const uint4 v0 = R.w[h][0], v1 = R.w[h][BITS == 4 ? 0 : 1];
-      const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t af[4];
-        dequant_w8(words[2 * j], words[2 * j + 1], m, af);
-        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
-      }
-    }
-  }
-}
-
-// Segment bookkeeping of one consumer warp: local index of the segment's
-// last tile, whether the segment covers its whole row block, and the block.
+// Segment bookkeeping of one warp: local index of the segment's last tile,
+// whether the segment covers its whole row block, and the block.
 struct Segment {
   int end, nb;
   bool whole;
@@ -289,22 +338,32 @@ __device__ __forceinline__ void next_segment(Segment& g, int ntile, int KT) {
   ++g.nb;
 }
 
-// Issue fill f of this CTA's ring (tiles 2f, 2f+1 of its range and their
-// activation slices) into slot s.  The activations are read only once the
-// grid dependency has resolved (x_ok).
-template <int TPS>
+// Issue fill f of this CTA's ring (tiles TPS*f .. of its range and their
+// activation slices) into stage s.  Called by all lanes of one warp: lane i
+// copies unit i % 8 of tile i / 8; lane 0 arms the barrier and loads the
+// activations.  The activations are read only once the grid dependency has
+// resolved (x).
+template <int BITS, int GPT, int TPS>
 __device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap* tmx, uint32_t sbase, uint32_t full,
-                                           long long t0, int ntile, int f, int s, bool weights, bool x) {
+                                           long long t0, int ntile, int f, int s, bool weights, bool x, int lane) {
+  constexpr int UB = unit_bytes_gpu(BITS, GPT);
   const int i = f * TPS;
   const int n = ntile - i < TPS ? ntile - i : TPS;
   const uint32_t x_bytes = (uint32_t)a.M * 256u;
   const uint32_t bar = full + 8u * s;
   const uint32_t dst = sbase + (uint32_t)(s * a.stage_bytes);
   if (weights) {
-    mbar_arrive_expect_tx(bar, (uint32_t)n * ((uint32_t)a.tile_bytes + x_bytes));
-    bulk_load(dst, a.tiles + (t0 + i) * a.tile_bytes, (uint32_t)(n * a.tile_bytes), bar);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n * ((uint32_t)(kSlabsPerTile * UB) + x_bytes));
+    __syncwarp();
+    if (lane < n * kSlabsPerTile) {
+      const int j = lane / kSlabsPerTile, mb = lane % kSlabsPerTile;
+      const long long tt = t0 + i + j;
+      const int nb = (int)(tt / a.KT), kt = (int)(tt - (long long)nb * a.KT);
+      bulk_load(dst + (uint32_t)(lane * UB), a.units + ((size_t)(nb * kSlabsPerTile + mb) * a.KT + kt) * UB,
+                (uint32_t)UB, bar);
+    }
   }
-  if (x) {
+  if (x && lane == 0) {
     for (int q = 0; q < n; ++q) {
       const int kt = (int)((t0 + i + q) % a.KT);
       tma_load_2d(dst + (uint32_t)a.x_off + (uint32_t)q * x_bytes, tmx, kt * kTileK, 0, bar);
@@ -316,66 +375,60 @@ template <int BITS, int GPT>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                const GemvArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* smem = align128(smem_raw);
+  constexpr int UB = unit_bytes_gpu(BITS, GPT);
+  constexpr int kTilesPerStage = tiles_per_stage(BITS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const long long t0 = tile_begin(c, a.T, a.G), t1 = tile_begin(c + 1, a.T, a.G);
   const int ntile = (int)(t1 - t0);
-  constexpr int kTilesPerStage = tiles_per_stage(BITS);
   const int nfill = (ntile + kTilesPerStage - 1) / kTilesPerStage;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full = sbase + (uint32_t)(a.NS * a.stage_bytes);
   const uint32_t empty = full + 8u * a.NS;
-  // per-slot release counters: the last warp to hand a slot back refills it
+  // per-stage release counters: the last warp to hand a stage back refills it
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.NS * a.stage_bytes + 16 * a.NS);
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full + 8 * i, 1);
-      mbar_init(empty + 8 * i, kGemvConsumers);
+      mbar_init(empty + 8 * i, kGemvWarps);
       released[i] = 0;
     }
     mbar_init_fence();
-    if (ntile > 0) {
-      griddep_launch_dependents();
-      prefetch_tensormap(&tmx);
-      // static weights first, before the grid dependency resolves
-      for (int f = 0; f < npre; ++f) issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, true, false);
-    }
   }
   __syncthreads();
   if (ntile <= 0) return;
+  if (warp == 0) {
+    if (lane == 0) {
+      griddep_launch_dependents();
+      prefetch_tensormap(&tmx);
+    }
+    // static weights first, before the grid dependency resolves
+    for (int f = 0; f < npre; ++f)
+      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, true, false, lane);
+  }
   // y, x and the workspace may still be in use by the previous grid
   griddep_wait();
-  if (threadIdx.x == 0)
-    for (int f = 0; f < npre; ++f) issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true);
+  if (warp == 0)
+    for (int f = 0; f < npre; ++f)
+      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true, lane);
 
   const int gr = lane >> 2, t = lane & 3;  // mma.sync fragment coordinates
-  constexpr int SB = BITS == 4 ? 16 : 32;
-  constexpr int WB = kTileN * kTileK * BITS / 8;
-  LaneOffsets o;
-  o.w = warp * 2 * 32 * SB + lane * SB;  // slot p = 4 gr + t = lane
-  o.s = WB + (warp * 8 + gr) * 4;
-  o.z = WB + GPT * 256 + (BITS == 4 ? (warp * 8 + gr) : (warp * 8 + gr) * 2);
-  o.gi0 = GPT == 1 ? 0 : (16 * t) / a.g;
-  o.gi1 = GPT == 1 ? 0 : (64 + 16 * t) / a.g;
-  o.x_on = gr < a.M;
-  o.x = (o.x_on ? gr : 0) * 256 + 32 * t;
+  (void)gr;
+  const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
   const int x_stride = a.M * 256;
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  TileRegs<BITS, GPT> R;
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int v = 0; v < 2; ++v) R.x[h][v] = make_uint4(0, 0, 0, 0);
+  UnitRegs<BITS, GPT> R;
+  clear_x(R);
   Segment seg = first_segment(t0, ntile, a.KT);
   // at most two segments of a contiguous range are partial: its first and its last
   int pending0 = 0, pending1 = 0, npending = 0;
   int s = 0;
   uint32_t lap = 0;
   for (int f = 0; f < nfill; ++f) {
-    if (!mbar_wait(full + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs)) break;
+    if (!warp_wait(full + 8 * s, lap & 1u, a.err)) break;
     const int i0 = f * kTilesPerStage;
     const int n = ntile - i0 < kTilesPerStage ? ntile - i0 : kTilesPerStage;
     const uint8_t* st = smem + s * a.stage_bytes;
@@ -383,22 +436,23 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 #pragma unroll
     for (int j = 0; j < kTilesPerStage; ++j) {
       if (j < n) {
-        load_tile(R, st + j * a.tile_bytes, xs + j * x_stride, o);
+        load_unit(R, st + (j * kSlabsPerTile + warp) * UB, xs + j * x_stride, o);
         if (j == n - 1) {
           // the whole stage has been read: hand it back; the last warp to do
           // so refills it
           __syncwarp();
+          unsigned refill = 0;
           if (lane == 0) {
             mbar_arrive(empty + 8 * s);
-            if (atomicAdd(released + s, 1u) == kGemvConsumers - 1) {
+            if (atomicAdd(released + s, 1u) == kGemvWarps - 1) {
               released[s] = 0;
-              if (f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs))
-                issue_fill<kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true);
+              refill = f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
             }
           }
-          __syncwarp();
+          if (__shfl_sync(0xFFFFFFFFu, refill, 0))
+            issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true, lane);
         }
-        mma_tile(R, acc);
+        mma_unit(R, acc);
         if (i0 + j == seg.end) {
           const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
                               acc[0][3] + acc[1][3]};
@@ -416,6 +470,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     }
     if (++s == a.NS) { s = 0; ++lap; }
   }
+  (void)t;
   if (npending > 0) {
     fence_acq_rel_gpu();  // release: this lane's partials before any count below
     __syncwarp();
@@ -424,40 +479,322 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   }
 }
 
-// Grid of the GEMV: two CTAs per SM, never more CTAs than tiles.
-struct GemvPlan {
-  long long T;
-  int G, S_max;
-  int NS, stage_bytes, x_off;
-  size_t smem, partial_bytes, counter_bytes;
+// ===========================================================================
+// slab GEMV (whole slabs per CTA, K split across the CTA's warps)
+//
+// CTA c owns slabs [c*spc, min((c+1)*spc, nslab)) — one contiguous byte
+// range of the blob — over all of K.  Its ring stage holds U = 8*UPW
+// consecutive units of one slab (one bulk copy).  The activations are
+// copied with 16-byte cp.async (load/store path, so they do not queue behind
+// weight copies already issued to the TMA unit): all of x once, into a
+// resident buffer, when it fits, else each stage's slices with the stage.
+// Warp w takes units w, w + 8, ... of every stage.  At the end of a slab
+// each warp parks its partial sums in a shared-memory slot; the last warp
+// to arrive adds the eight in warp order and writes 16 rows of y, so no warp
+// waits for another.
+
+__host__ __device__ constexpr int slab_units_per_warp(int bits) { return bits == 4 ? 2 : 1; }
+
+struct SlabArgs {
+  const uint8_t* units;
+  const uint16_t* x;
+  uint16_t* y;
+  unsigned* err;
+  int N, K, M, KT, g;
+  int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
+  int x_res;            // 1: x resident in shared memory; 0: x slices travel with each stage
+  int R;                // reduction slots (a warp is never more than R - 1 slabs ahead of another)
+  int NS, stage_bytes, x_off, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
 };
 
-constexpr int kGemvSmemBudget = 110 * 1024;  // ring bytes per CTA; two CTAs share an SM
+// 16-byte chunks r in [r0, r1) (stepping by `step`) of the activation columns
+// [128*k0, 128*(k0 + n)) for every token, into [unit][token][128] at dst;
+// columns past K are zero-filled.
+__device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int k0, int n, int r0, int step) {
+  const int per_m = n * 16;
+  for (int m = 0; m < a.M; ++m) {
+    const uint16_t* xm = a.x + (size_t)m * a.K;
+    for (int r = r0; r < per_m; r += step) {
+      const int col = (k0 * kTileK) + 8 * r;
+      const bool in = col < a.K;
+      cp_async_16(dst + (uint32_t)((r >> 4) * a.M * 256 + m * 256 + (r & 15) * 16), xm + (in ? col : 0),
+                  in ? 16u : 0u);
+    }
+  }
+}
+
+// Fill f of the CTA whose first slab is s0: units [U*q, U*q + n) of slab
+// s0 + f / QPS (q = f % QPS) into stage st.  Weights: one bulk copy issued
+// by lane 0.  Per-stage activations (x_res == 0): all 32 lanes copy 16-byte
+// chunks and each lane then arrives on the stage's barrier once its copies
+// have landed (the barrier then expects 1 + 32 arrivals per fill).
+template <int BITS, int GPT>
+__device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uint32_t full, int s0, int f, int st,
+                                          bool weights, bool x, int lane) {
+  constexpr int UB = unit_bytes_gpu(BITS, GPT);
+  constexpr int U = kGemvWarps * slab_units_per_warp(BITS);
+  const int qs = f / a.QPS;
+  const int sl = s0 + qs, k0 = (f - qs * a.QPS) * U;
+  const int n = a.KT - k0 < U ? a.KT - k0 : U;
+  const uint32_t bar = full + 8u * st;
+  const uint32_t dst = sbase + (uint32_t)(st * a.stage_bytes);
+  if (weights && lane == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(n * UB));
+    bulk_load(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar);
+  }
+  if (x && !a.x_res) {
+    copy_x(a, dst + (uint32_t)a.x_off, k0, n, lane, 32);
+    cp_async_mbar_arrive_noinc(bar);
+  }
+}
+
+template <int BITS, int GPT>
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align128(smem_raw);
+  constexpr int UB = unit_bytes_gpu(BITS, GPT);
+  constexpr int UPW = slab_units_per_warp(BITS);
+  constexpr int U = kGemvWarps * UPW;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 2, t = lane & 3;
+  const int s0 = blockIdx.x * a.spc;
+  const int ns = a.nslab - s0 < a.spc ? a.nslab - s0 : a.spc;  // >= 1 for every CTA of the grid
+  const int nfill = ns * a.QPS;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full = sbase + (uint32_t)a.ctl_off;
+  const uint32_t empty = full + 8u * a.NS;
+  unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 16 * a.NS);
+  unsigned* red_cnt = released + a.NS;                   // [R] warps that parked a partial
+  volatile unsigned* red_gen = red_cnt + a.R;            // [R] slabs reduced in this slot so far
+  int* ctl = reinterpret_cast<int*>(red_cnt + 2 * a.R);  // [0] fills issued, [1] some wait ran out
+  float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [R][8 warps][32 lanes]
+  const int npre = nfill < a.NS ? nfill : a.NS;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.NS; ++i) {
+      mbar_init(full + 8 * i, a.x_res ? 1 : 1 + 32);
+      mbar_init(empty + 8 * i, kGemvWarps);
+      released[i] = 0;
+    }
+    for (int i = 0; i < a.R; ++i) {
+      red_cnt[i] = 0;
+      red_gen[i] = 0;
+    }
+    ctl[0] = npre;
+    ctl[1] = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) griddep_launch_dependents();
+    // static weights first, before the grid dependency resolves
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT>(a, sbase, full, s0, f, f, true, false, lane);
+  }
+  // y and x may still be in use by the previous grid
+  griddep_wait();
+  if (a.x_res) {
+    copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, kGemvThreads);
+    cp_async_wait_all();
+    __syncthreads();
+  } else if (warp == 0) {
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT>(a, sbase, full, s0, f, f, false, true, lane);
+  }
+
+  const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
+  const int x_unit = a.M * 256;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  UnitRegs<BITS, GPT> R[UPW];
+#pragma unroll
+  for (int j = 0; j < UPW; ++j) clear_x(R[j]);
+  bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
+  int st = 0, q = 0, si = 0;
+  uint32_t lap = 0;
+  for (int f = 0; f < nfill; ++f) {
+    const int k0 = q * U;
+    const int n = a.KT - k0 < U ? a.KT - k0 : U;
+    if (!dead && !warp_wait(full + 8 * st, lap & 1u, a.err)) dead = true;
+    const uint8_t* stp = smem + st * a.stage_bytes;
+    const uint8_t* xp = a.x_res ? smem + a.xres_off + k0 * x_unit : stp + a.x_off;
+    if (!dead) {
+#pragma unroll
+      for (int j = 0; j < UPW; ++j) {
+        const int u = j * kGemvWarps + warp;
+        if (u < n) load_unit(R[j], stp + u * UB, xp + u * x_unit, o);
+      }
+    }
+    // the stage has been read: hand it back; the last warp to do so refills it
+    __syncwarp();
+    unsigned refill = 0;
+    if (lane == 0) {
+      mbar_arrive(empty + 8 * st);
+      if (atomicAdd(released + st, 1u) == kGemvWarps - 1) {
+        released[st] = 0;
+        refill = !dead && f + a.NS < nfill &&
+                 mbar_wait(empty + 8 * st, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
+        if (refill) atomicAdd(ctl, 1);
+      }
+    }
+    if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+    if (!dead) {
+#pragma unroll
+      for (int j = 0; j < UPW; ++j)
+        if (j * kGemvWarps + warp < n) mma_unit(R[j], acc);
+    }
+    if (++q == a.QPS) {
+      // Slab s0 + si is done for this warp: park the partial sums in slot
+      // si % R; the eighth warp to do so adds them in warp order.
+      const int slot = si % a.R;
+      const unsigned gen = (unsigned)(si / a.R);
+      int bad = 0;
+      if (lane == 0) {
+        if (red_gen[slot] != gen) {
+          // the slot's previous slab is still being reduced (cannot happen
+          // while R exceeds the ring's reach, but never overwrite it)
+          const uint64_t tw = global_timer_ns();
+          while (red_gen[slot] != gen) {
+            if (global_timer_ns() - tw > kGemvTimeoutNs) {
+              atomicCAS(a.err, 0u, kErrGemvWait);
+              bad = 1;
+              break;
+            }
+          }
+        }
+        __threadfence_block();  // acquire: the previous reduction has finished reading the slot
+      }
+      __syncwarp();
+      if (__shfl_sync(0xFFFFFFFFu, bad, 0)) dead = true;
+      float4* rb = red + slot * (kGemvWarps * 32);
+      rb[warp * 32 + lane] = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
+                                         acc[0][3] + acc[1][3]);
+      __syncwarp();
+      unsigned last = 0;
+      if (lane == 0) {
+        __threadfence_block();  // release this warp's partials
+        last = atomicAdd(red_cnt + slot, 1u) == kGemvWarps - 1;
+        __threadfence_block();  // acquire the other warps' partials
+      }
+      __syncwarp();
+      if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) {
+          const float4 u = rb[w * 32 + lane];
+          v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+        }
+        if (!dead) store_y(a.y, a.N, a.M, (s0 + si) * kSlabN + gr, t, v);
+        __syncwarp();
+        if (lane == 0) {
+          red_cnt[slot] = 0;
+          __threadfence_block();
+          red_gen[slot] = gen + 1;  // the slot is free for slab si + R
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
+      q = 0;
+      ++si;
+    }
+    if (++st == a.NS) { st = 0; ++lap; }
+  }
+  if (dead && lane == 0) atomicOr(ctl + 1, 1);
+  __syncthreads();
+  if (threadIdx.x == 0 && ctl[1]) {
+    // A wait ran out: let the copies still in flight land before the CTA's
+    // shared memory goes away.  Only the last NS fills can be outstanding.
+    const int issued = ctl[0];
+    for (int f = issued > a.NS ? issued - a.NS : 0; f < issued; ++f)
+      mbar_wait(full + 8 * (f % a.NS), (uint32_t)(f / a.NS) & 1u, a.err, kErrGemvWait, kGemvDrainNs);
+  }
+}
+
+// ===========================================================================
+// host side
+
+constexpr int kGemvSmemBudget = 110 * 1024;  // ring + control bytes per CTA; two CTAs share an SM
 constexpr int kGemvSmemMax = 113 * 1024;
 
+struct GemvPlan {
+  bool slab;  // slab GEMV (else tile GEMV)
+  int G;      // CTAs
+  int NS, stage_bytes, x_off;
+  // tile GEMV
+  long long T;
+  int S_max;
+  size_t partial_bytes, counter_bytes;
+  // slab GEMV
+  int nslab, spc, QPS, x_res, R, xres_off, red_off, ctl_off;
+  size_t smem;
+};
+
+inline int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// Deepest slab-GEMV ring (<= 16 stages) that fits the budget next to the
+// resident x (xres bytes, 0 if none), the reduction slots and the control
+// words; 0 if not even two stages fit.
+inline int slab_ring(GemvPlan* P, int stage, int xres) {
+  for (int ns = 16; ns >= 2; --ns) {
+    const int R = clampi((ns - 1 + P->QPS - 1) / P->QPS + 2, 2, 16);
+    const int red = R * kGemvWarps * 32 * 16;
+    const int ctl = 16 * ns + 4 * ns + 8 * R + 8;
+    if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
+      P->NS = ns;
+      P->R = R;
+      P->stage_bytes = stage;
+      P->xres_off = ns * stage;
+      P->red_off = P->xres_off + xres;
+      P->ctl_off = P->red_off + red;
+      P->smem = 128 + (size_t)P->ctl_off + ctl;
+      return ns;
+    }
+  }
+  return 0;
+}
+
 inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
-  const int kTilesPerStage = tiles_per_stage(Gm.bits);
   const int sms = sm_count();
   if (sms <= 0) return TF_ERR_CUDA;
+  *P = GemvPlan{};
+  const int nslab = (Gm.N + kSlabN - 1) / kSlabN;
+  if (nslab >= sms && Gm.KT >= kGemvWarps) {
+    // Enough slabs for every SM: whole slabs per CTA, at most two CTAs per SM.
+    const int U = kGemvWarps * slab_units_per_warp(Gm.bits);
+    const int slots = 2 * sms;
+    P->slab = true;
+    P->nslab = nslab;
+    P->spc = (nslab + slots - 1) / slots;
+    P->G = (nslab + P->spc - 1) / P->spc;
+    P->QPS = (Gm.KT + U - 1) / U;
+    const int wbytes = (U * Gm.unit_bytes + 127) / 128 * 128;
+    // x resident in shared memory if that still leaves a ring of 4 stages
+    const int xres = (Gm.KT * M * 256 + 127) / 128 * 128;
+    P->x_off = wbytes;
+    P->x_res = slab_ring(P, wbytes, xres) >= 4;
+    if (P->x_res || slab_ring(P, wbytes + U * M * 256, 0) > 0) return TF_OK;
+    *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
+  }
+  const int TPS = tiles_per_stage(Gm.bits);
+  P->slab = false;
   P->T = (long long)Gm.NB * Gm.KT;
   P->G = (int)(P->T < 2LL * sms ? P->T : 2LL * sms);
   const long long per_cta = (P->T + P->G - 1) / P->G;
   P->S_max = (int)((per_cta + Gm.KT - 1) / Gm.KT + 1);
   P->partial_bytes = (size_t)P->G * P->S_max * 8 * 32 * sizeof(float4);
   P->counter_bytes = ((size_t)Gm.NB * 8 * sizeof(unsigned) + 255) / 256 * 256;
-  P->x_off = (kTilesPerStage * Gm.tile_bytes + 127) / 128 * 128;
-  P->stage_bytes = P->x_off + kTilesPerStage * M * 256;
-  int ns = kGemvSmemBudget / P->stage_bytes;
-  P->NS = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+  P->x_off = (TPS * kSlabsPerTile * Gm.unit_bytes + 127) / 128 * 128;
+  P->stage_bytes = P->x_off + TPS * M * 256;
+  P->NS = clampi(kGemvSmemBudget / P->stage_bytes, 2, 6);
   P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS;
   return TF_OK;
 }
 
-template <int BITS, int GPT>
-int launch_gemv(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
-  auto kfn = gemv_kernel<BITS, GPT>;
-  // Opt in once per device to the largest ring gemv_plan can ask for.
-  static std::atomic<unsigned long long> opted{0};
+inline size_t gemv_scratch_bytes(const GemvPlan& P) { return P.slab ? 0 : P.partial_bytes + P.counter_bytes; }
+
+// Launch with programmatic dependent launch; opts the kernel in, once per
+// device, to the largest ring a plan can ask for.
+template <class Kern, class... Args>
+int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, size_t smem, cudaStream_t s,
+               Args... args) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
   if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
@@ -468,7 +805,7 @@ int launch_gemv(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStre
   }
   if (smem > (size_t)kGemvSmemMax) return TF_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.G);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kGemvThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -477,7 +814,7 @@ int launch_gemv(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kfn, map, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kfn, args...) != cudaSuccess) {
     cudaGetLastError();
     return TF_ERR_CUDA;
   }
@@ -485,8 +822,62 @@ int launch_gemv(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStre
 }
 
 template <int BITS, int GPT>
-void launch_dequant(const uint8_t* tiles, const Geometry& G, uint16_t* w, cudaStream_t s) {
-  dequant_kernel<BITS, GPT><<<G.NB * G.KT, 512, 0, s>>>(tiles, G.N, G.K, G.KT, G.g, G.tile_bytes, w);
+int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
+  static std::atomic<unsigned long long> opted{0};
+  return launch_pdl(gemv_kernel<BITS, GPT>, opted, a.G, smem, s, map, a);
+}
+
+template <int BITS, int GPT>
+int launch_slab(const SlabArgs& a, int grid, size_t smem, cudaStream_t s) {
+  static std::atomic<unsigned long long> opted{0};
+  return launch_pdl(gemv_slab_kernel<BITS, GPT>, opted, grid, smem, s, a);
+}
+
+// The GEMV of a checked layer with a plan; partials / counters are the
+// tile GEMV's scratch (unused by the slab GEMV).
+int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint16_t* x, uint16_t* y, int M,
+             float4* partials, unsigned* counters, cudaStream_t stream) {
+  unsigned* err = device_error_ptr();
+  if (!err) return TF_ERR_CUDA;
+  const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  if (P.slab) {
+    SlabArgs a;
+    a.units = units; a.x = x; a.y = y; a.err = err;
+    a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
+    a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS; a.x_res = P.x_res; a.R = P.R;
+    a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off; a.xres_off = P.xres_off;
+    a.red_off = P.red_off; a.ctl_off = P.ctl_off;
+    if (G.bits == 4) {
+      if (G.gpt == 1) return launch_slab<4, 1>(a, P.G, P.smem, stream);
+      if (G.gpt == 2) return launch_slab<4, 2>(a, P.G, P.smem, stream);
+      return launch_slab<4, 4>(a, P.G, P.smem, stream);
+    }
+    if (G.gpt == 1) return launch_slab<8, 1>(a, P.G, P.smem, stream);
+    if (G.gpt == 2) return launch_slab<8, 2>(a, P.G, P.smem, stream);
+    return launch_slab<8, 4>(a, P.G, P.smem, stream);
+  }
+  CUtensorMap map;
+  int rc = encode_x_map(x, M, G.K, &map);
+  if (rc) return rc;
+  GemvArgs a;
+  a.units = units; a.y = y; a.partials = partials; a.counters = counters; a.err = err;
+  a.T = P.T;
+  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
+  a.G = P.G; a.S_max = P.S_max;
+  a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
+  if (G.bits == 4) {
+    if (G.gpt == 1) return launch_tile<4, 1>(map, a, P.smem, stream);
+    if (G.gpt == 2) return launch_tile<4, 2>(map, a, P.smem, stream);
+    return launch_tile<4, 4>(map, a, P.smem, stream);
+  }
+  if (G.gpt == 1) return launch_tile<8, 1>(map, a, P.smem, stream);
+  if (G.gpt == 2) return launch_tile<8, 2>(map, a, P.smem, stream);
+  return launch_tile<8, 4>(map, a, P.smem, stream);
+}
+
+template <int BITS, int GPT>
+void launch_dequant(const uint8_t* units, const Geometry& G, uint16_t* w, cudaStream_t s) {
+  dequant_kernel<BITS, GPT><<<G.NB * G.KT, 512, 0, s>>>(units, G.N, G.K, G.KT, G.g, w);
 }
 
 }  // namespace
@@ -503,15 +894,15 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
   if (rc) return rc;
   if (!w) return TF_ERR_INVALID_ARG;
   if (!aligned16(w)) return TF_ERR_ALIGNMENT;
-  const uint8_t* tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   if (bits == 4) {
-    if (G.gpt == 1) launch_dequant<4, 1>(tiles, G, w, stream);
-    else if (G.gpt == 2) launch_dequant<4, 2>(tiles, G, w, stream);
-    else launch_dequant<4, 4>(tiles, G, w, stream);
+    if (G.gpt == 1) launch_dequant<4, 1>(units, G, w, stream);
+    else if (G.gpt == 2) launch_dequant<4, 2>(units, G, w, stream);
+    else launch_dequant<4, 4>(units, G, w, stream);
   } else {
-    if (G.gpt == 1) launch_dequant<8, 1>(tiles, G, w, stream);
-    else if (G.gpt == 2) launch_dequant<8, 2>(tiles, G, w, stream);
-    else launch_dequant<8, 4>(tiles, G, w, stream);
+    if (G.gpt == 1) launch_dequant<8, 1>(units, G, w, stream);
+    else if (G.gpt == 2) launch_dequant<8, 2>(units, G, w, stream);
+    else launch_dequant<8, 4>(units, G, w, stream);
   }
   return launch_status();
 }
@@ -526,7 +917,7 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
-  *bytes = P.partial_bytes + P.counter_bytes;
+  *bytes = gemv_scratch_bytes(P);
   return TF_OK;
 }
 
@@ -541,31 +932,12 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
-  if (!workspace || workspace_bytes < P.partial_bytes + P.counter_bytes) return TF_ERR_WORKSPACE;
-  CUtensorMap map;
-  rc = encode_x_map(x, M, K, &map);
-  if (rc) return rc;
-  GemvArgs a;
-  a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
-  a.y = y;
-  a.partials = static_cast<float4*>(workspace);
-  a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes);
-  a.err = device_error_ptr();
-  if (!a.err) return TF_ERR_CUDA;
-  a.T = P.T;
-  a.N = N; a.K = K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
-  a.G = P.G; a.S_max = P.S_max;
-  a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
-  if (bits == 4) {
-    if (G.gpt == 1) return launch_gemv<4, 1>(map, a, P.smem, stream);
-    if (G.gpt == 2) return launch_gemv<4, 2>(map, a, P.smem, stream);
-    return launch_gemv<4, 4>(map, a, P.smem, stream);
-  }
-  if (G.gpt == 1) return launch_gemv<8, 1>(map, a, P.smem, stream);
-  if (G.gpt == 2) return launch_gemv<8, 2>(map, a, P.smem, stream);
-  return launch_gemv<8, 4>(map, a, P.smem, stream);
+  const size_t need = gemv_scratch_bytes(P);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
+  return run_gemv(G, P, blob, x, y, M, static_cast<float4*>(workspace),
+                  need ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes) : nullptr,
+                  stream);
 }
-
 
 // ===========================================================================
 // tf_gemv_noalloc: tf_gemv with its scratch in a fixed device array.
@@ -573,12 +945,13 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
 // Some callers cannot allocate device memory at the point where they run a
 // layer: code that runs inside another framework's memory pool, plugins
 // handed only input and output pointers, or real-time paths where an
-// allocation may block or fail.  For them the split-K scratch of the GEMV
-// (FP32 partial sums + arrival counters) lives in this file-scope array,
-// which every GPU that loads the library holds until the process exits.
-// Host code must not pass the array's name to a kernel (on the host it is
-// only a stand-in): its device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current.
+// allocation may block or fail.  For them the split-K scratch of the tile
+// GEMV (FP32 partial sums + arrival counters) lives in this file-scope
+// array, which every GPU that loads the library holds until the process
+// exits; the slab GEMV needs none.  Host code must not pass the array's name
+// to a kernel (on the host it is only a stand-in): its device address is
+// looked up once per device with cudaGetSymbolAddress, with that device
+// current.
 
 }  // extern "C"
 
@@ -614,35 +987,16 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
-  if (P.partial_bytes + P.counter_bytes > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
+  if (gemv_scratch_bytes(P) > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
+  if (P.slab) return run_gemv(G, P, blob, x, y, M, nullptr, nullptr, stream);
   unsigned char* scratch = gemv_scratch_address();
   if (!scratch) return TF_ERR_CUDA;
   // The arrival counters must start at zero; a call cut short (device error)
   // could have left them dirty, so clear them on the stream first.
   unsigned char* counters = scratch + P.partial_bytes;
   if (cudaMemsetAsync(counters, 0, P.counter_bytes, stream) != cudaSuccess) return TF_ERR_CUDA;
-  CUtensorMap map;
-  rc = encode_x_map(x, M, K, &map);
-  if (rc) return rc;
-  GemvArgs a;
-  a.tiles = static_cast<const uint8_t*>(blob) + kHeaderBytes;
-  a.y = y;
-  a.partials = reinterpret_cast<float4*>(scratch);
-  a.counters = reinterpret_cast<unsigned*>(counters);
-  a.err = device_error_ptr();
-  if (!a.err) return TF_ERR_CUDA;
-  a.T = P.T;
-  a.N = N; a.K = K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = G.tile_bytes;
-  a.G = P.G; a.S_max = P.S_max;
-  a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
-  if (bits == 4) {
-    if (G.gpt == 1) return launch_gemv<4, 1>(map, a, P.smem, stream);
-    if (G.gpt == 2) return launch_gemv<4, 2>(map, a, P.smem, stream);
-    return launch_gemv<4, 4>(map, a, P.smem, stream);
-  }
-  if (G.gpt == 1) return launch_gemv<8, 1>(map, a, P.smem, stream);
-  if (G.gpt == 2) return launch_gemv<8, 2>(map, a, P.smem, stream);
-  return launch_gemv<8, 4>(map, a, P.smem, stream);
+  return run_gemv(G, P, blob, x, y, M, reinterpret_cast<float4*>(scratch), reinterpret_cast<unsigned*>(counters),
+                  stream);
 }
 
 }  // extern "C"

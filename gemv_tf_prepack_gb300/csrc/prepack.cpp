@@ -45,58 +45,53 @@ struct Source {
   }
 };
 
-// Tile row / column of code i of word j in slot p of block (mb, h).
-inline void code_position(int mb, int h, int p, int j, int i, int* row, int* col) {
+// Unit row / column of code i of word j in slot p of K half h.
+inline void code_position(int h, int p, int j, int i, int* row, int* col) {
   const int gr = p >> 2, t = p & 3, r = i & 3, e = i >> 2;
-  *row = mb * 16 + gr + 8 * (r & 1);
+  *row = gr + 8 * (r & 1);
   *col = h * 64 + 16 * t + 4 * j + 2 * (r >> 1) + e;
 }
 
-void pack_tile(const Source& src, int nb, int kt, uint8_t* tile) {
+void pack_unit(const Source& src, int s, int kt, uint8_t* unit) {
   const Geometry& G = src.G;
   const int sb = tf::slot_bytes(G.bits);
-  for (int mb = 0; mb < 8; ++mb)
-    for (int h = 0; h < 2; ++h)
-      for (int p = 0; p < 32; ++p) {
-        uint8_t* slot = tile + ((mb * 2 + h) * 32 + p) * sb;
-        for (int j = 0; j < 4; ++j) {
-          uint32_t word = 0;
-          for (int i = 0; i < 8; ++i) {
-            int row, col;
-            code_position(mb, h, p, j, i, &row, &col);
-            const int c = src.padded_code(nb * tf::kTileN + row, kt * tf::kTileK + col);
-            if (G.bits == 4)
-              word |= (uint32_t)c << (4 * i);
-            else
-              slot[8 * j + i] = (uint8_t)c;
-          }
-          if (G.bits == 4) {
-            for (int b = 0; b < 4; ++b) slot[4 * j + b] = (uint8_t)(word >> (8 * b));
-          }
+  for (int h = 0; h < 2; ++h)
+    for (int p = 0; p < 32; ++p) {
+      uint8_t* slot = unit + (h * 32 + p) * sb;
+      for (int j = 0; j < 4; ++j) {
+        uint32_t word = 0;
+        for (int i = 0; i < 8; ++i) {
+          int row, col;
+          code_position(h, p, j, i, &row, &col);
+          const int c = src.padded_code(s * tf::kSlabN + row, kt * tf::kTileK + col);
+          if (G.bits == 4)
+            word |= (uint32_t)c << (4 * i);
+          else
+            slot[8 * j + i] = (uint8_t)c;
+        }
+        if (G.bits == 4) {
+          for (int b = 0; b < 4; ++b) slot[4 * j + b] = (uint8_t)(word >> (8 * b));
         }
       }
-  uint8_t* sptr = tile + tf::tile_weight_bytes(G.bits);
-  uint8_t* zptr = sptr + 256 * G.gpt;
-  const int zb = tf::tile_zero_bytes(G.bits);
+    }
   for (int gi = 0; gi < G.gpt; ++gi) {
     const int grp = src.group_of(kt * tf::kTileK + (G.gpt > 1 ? gi * G.g : 0));
-    for (int mb = 0; mb < 8; ++mb)
-      for (int gr = 0; gr < 8; ++gr)
-        for (int e = 0; e < 2; ++e) {
-          const int n = nb * tf::kTileN + mb * 16 + gr + 8 * e;
-          const uint16_t s = src.scale(n, grp);
-          uint8_t* d = sptr + gi * 256 + ((mb * 8 + gr) * 2 + e) * 2;
-          d[0] = (uint8_t)(s & 0xFF);
-          d[1] = (uint8_t)(s >> 8);
-          const uint8_t z = src.zero(n, grp);
-          if (G.bits == 4) {
-            uint8_t& zz = zptr[gi * zb + mb * 8 + gr];
-            if (e == 0) zz = (uint8_t)((zz & 0xF0) | z);
-            else zz = (uint8_t)((zz & 0x0F) | (z << 4));
-          } else {
-            zptr[gi * zb + (mb * 8 + gr) * 2 + e] = z;
-          }
+    for (int gr = 0; gr < 8; ++gr)
+      for (int e = 0; e < 2; ++e) {
+        const int n = s * tf::kSlabN + gr + 8 * e;
+        const uint16_t sc = src.scale(n, grp);
+        uint8_t* d = unit + tf::unit_scale_offset(G.bits, gi, gr) + 2 * e;
+        d[0] = (uint8_t)(sc & 0xFF);
+        d[1] = (uint8_t)(sc >> 8);
+        const uint8_t z = src.zero(n, grp);
+        uint8_t* zp = unit + tf::unit_zero_offset(G.bits, G.gpt, gi, gr);
+        if (G.bits == 4) {
+          if (e == 0) *zp = (uint8_t)((*zp & 0xF0) | z);
+          else *zp = (uint8_t)((*zp & 0x0F) | (z << 4));
+        } else {
+          zp[e] = z;
         }
+      }
   }
 }
 
@@ -106,24 +101,25 @@ void write_header(const Geometry& G, uint8_t* out) {
   h.magic = tf::kMagic;
   h.version = tf::kVersion;
   h.N = G.N; h.K = G.K; h.bits = G.bits; h.group = G.group;
-  h.tile_n = tf::kTileN; h.tile_k = tf::kTileK;
-  h.NB = G.NB; h.KT = G.KT; h.tile_bytes = G.tile_bytes; h.groups_per_tile = G.gpt;
+  h.unit_n = tf::kSlabN; h.unit_k = tf::kTileK;
+  h.S = G.S; h.KT = G.KT; h.unit_bytes = G.unit_bytes; h.groups_per_unit = G.gpt;
   h.total_bytes = G.total_bytes;
   std::memcpy(out, &h, sizeof h);  // the ABI is little-endian
 }
 
+// f(s) for every slab s, on up to 32 host threads.
 template <class F>
-void parallel_rows(int NB, F&& f) {
+void parallel_slabs(int S, F&& f) {
   unsigned nt = std::max(1u, std::min(std::thread::hardware_concurrency(), 32u));
-  nt = std::min<unsigned>(nt, (unsigned)NB);
+  nt = std::min<unsigned>(nt, (unsigned)S);
   if (nt <= 1) {
-    for (int nb = 0; nb < NB; ++nb) f(nb);
+    for (int s = 0; s < S; ++s) f(s);
     return;
   }
   std::vector<std::thread> th;
   for (unsigned w = 0; w < nt; ++w)
     th.emplace_back([&, w] {
-      for (int nb = (int)w; nb < NB; nb += (int)nt) f(nb);
+      for (int s = (int)w; s < S; s += (int)nt) f(s);
     });
   for (auto& t : th) t.join();
 }
@@ -173,11 +169,11 @@ int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros
   Source src{G, (const uint8_t*)qweight, (const uint32_t*)qweight, scales, zeros, n_groups};
   uint8_t* o = (uint8_t*)out;
   write_header(G, o);
-  parallel_rows(G.NB, [&](int nb) {
+  parallel_slabs(G.S, [&](int s) {
     for (int kt = 0; kt < G.KT; ++kt) {
-      uint8_t* tile = o + tf::kHeaderBytes + ((size_t)nb * G.KT + kt) * G.tile_bytes;
-      std::memset(tile, 0, G.tile_bytes);
-      pack_tile(src, nb, kt, tile);
+      uint8_t* unit = o + tf::unit_offset(G, s, kt);
+      std::memset(unit, 0, G.unit_bytes);
+      pack_unit(src, s, kt, unit);
     }
   });
   return TF_OK;
@@ -190,8 +186,8 @@ int tf_blob_info(const void* header, size_t bytes, int* N, int* K, int* bits, in
   if (h.magic != tf::kMagic || h.version != tf::kVersion) return TF_ERR_BAD_BLOB;
   Geometry G;
   if (tf::make_geometry(h.N, h.K, h.bits, h.group, &G)) return TF_ERR_BAD_BLOB;
-  if (h.tile_n != tf::kTileN || h.tile_k != tf::kTileK || h.NB != G.NB || h.KT != G.KT ||
-      h.tile_bytes != G.tile_bytes || h.groups_per_tile != G.gpt || h.total_bytes != G.total_bytes)
+  if (h.unit_n != tf::kSlabN || h.unit_k != tf::kTileK || h.S != G.S || h.KT != G.KT ||
+      h.unit_bytes != G.unit_bytes || h.groups_per_unit != G.gpt || h.total_bytes != G.total_bytes)
     return TF_ERR_BAD_BLOB;
   if (N) *N = h.N;
   if (K) *K = h.K;
@@ -211,49 +207,44 @@ int tf_unprepack(const void* blob, size_t bytes, void* qweight, uint16_t* scales
   const uint8_t* b = (const uint8_t*)blob;
   const int n_groups = K / G.g;
   const int sb = tf::slot_bytes(bits);
-  const int zb = tf::tile_zero_bytes(bits);
   if (bits == 4) std::memset(qweight, 0, (size_t)N * (K / 8) * 4);
-  parallel_rows(G.NB, [&](int nb) {
+  // Slab s only holds rows s*16 .. s*16+15: no two slabs write the same word.
+  parallel_slabs(G.S, [&](int s) {
+    if (s * tf::kSlabN >= N) return;
     for (int kt = 0; kt < G.KT; ++kt) {
-      const uint8_t* tile = b + tf::kHeaderBytes + ((size_t)nb * G.KT + kt) * G.tile_bytes;
-      for (int mb = 0; mb < 8; ++mb)
-        for (int h = 0; h < 2; ++h)
-          for (int p = 0; p < 32; ++p) {
-            const uint8_t* slot = tile + ((mb * 2 + h) * 32 + p) * sb;
-            for (int j = 0; j < 4; ++j)
-              for (int i = 0; i < 8; ++i) {
-                int row, col;
-                code_position(mb, h, p, j, i, &row, &col);
-                const int n = nb * tf::kTileN + row, k = kt * tf::kTileK + col;
-                if (n >= N || k >= K) continue;
-                int c;
-                if (bits == 4) {
-                  const uint32_t w = (uint32_t)slot[4 * j] | ((uint32_t)slot[4 * j + 1] << 8) |
-                                     ((uint32_t)slot[4 * j + 2] << 16) | ((uint32_t)slot[4 * j + 3] << 24);
-                  c = (w >> (4 * i)) & 0xF;
-                  ((uint32_t*)qweight)[(size_t)n * (K / 8) + (k >> 3)] |= (uint32_t)c << (4 * (k & 7));
-                } else {
-                  ((uint8_t*)qweight)[(size_t)n * K + k] = slot[8 * j + i];
-                }
+      const uint8_t* unit = b + tf::unit_offset(G, s, kt);
+      for (int h = 0; h < 2; ++h)
+        for (int p = 0; p < 32; ++p) {
+          const uint8_t* slot = unit + (h * 32 + p) * sb;
+          for (int j = 0; j < 4; ++j)
+            for (int i = 0; i < 8; ++i) {
+              int row, col;
+              code_position(h, p, j, i, &row, &col);
+              const int n = s * tf::kSlabN + row, k = kt * tf::kTileK + col;
+              if (n >= N || k >= K) continue;
+              if (bits == 4) {
+                const uint32_t w = (uint32_t)slot[4 * j] | ((uint32_t)slot[4 * j + 1] << 8) |
+                                   ((uint32_t)slot[4 * j + 2] << 16) | ((uint32_t)slot[4 * j + 3] << 24);
+                const int c = (w >> (4 * i)) & 0xF;
+                ((uint32_t*)qweight)[(size_t)n * (K / 8) + (k >> 3)] |= (uint32_t)c << (4 * (k & 7));
+              } else {
+                ((uint8_t*)qweight)[(size_t)n * K + k] = slot[8 * j + i];
               }
-          }
-      const uint8_t* sptr = tile + tf::tile_weight_bytes(bits);
-      const uint8_t* zptr = sptr + 256 * G.gpt;
+            }
+        }
       for (int gi = 0; gi < G.gpt; ++gi) {
         const int c0 = kt * tf::kTileK + (G.gpt > 1 ? gi * G.g : 0);
         if (c0 >= K) continue;
         const int grp = c0 / G.g;
-        for (int mb = 0; mb < 8; ++mb)
-          for (int gr = 0; gr < 8; ++gr)
-            for (int e = 0; e < 2; ++e) {
-              const int n = nb * tf::kTileN + mb * 16 + gr + 8 * e;
-              if (n >= N) continue;
-              const uint8_t* d = sptr + gi * 256 + ((mb * 8 + gr) * 2 + e) * 2;
-              scales[(size_t)n * n_groups + grp] = (uint16_t)(d[0] | (d[1] << 8));
-              zeros[(size_t)n * n_groups + grp] =
-                  bits == 4 ? (uint8_t)((zptr[gi * zb + mb * 8 + gr] >> (4 * e)) & 0xF)
-                            : zptr[gi * zb + (mb * 8 + gr) * 2 + e];
-            }
+        for (int gr = 0; gr < 8; ++gr)
+          for (int e = 0; e < 2; ++e) {
+            const int n = s * tf::kSlabN + gr + 8 * e;
+            if (n >= N) continue;
+            const uint8_t* d = unit + tf::unit_scale_offset(bits, gi, gr) + 2 * e;
+            scales[(size_t)n * n_groups + grp] = (uint16_t)(d[0] | (d[1] << 8));
+            const uint8_t* zp = unit + tf::unit_zero_offset(bits, G.gpt, gi, gr);
+            zeros[(size_t)n * n_groups + grp] = bits == 4 ? (uint8_t)((*zp >> (4 * e)) & 0xF) : zp[e];
+          }
       }
     }
   });

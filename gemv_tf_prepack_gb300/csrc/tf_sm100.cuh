@@ -68,6 +68,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
+// mbar_wait by every lane of a warp, with one result for the whole warp (a
+// lane that gave up makes the warp give up).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned* err, unsigned code,
+                                               uint64_t timeout_ns) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, err, code, timeout_ns));
+}
+
 // ---------------------------------------------------------------------------
 // bulk copies (global -> shared), completion counted on an mbarrier
 
@@ -85,6 +92,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+
+// 16-byte global -> shared copy through the load/store path (not the TMA
+// unit, so it does not queue behind bulk copies already issued); bytes past
+// src_bytes (0 or 16) are zero-filled.  Goes through L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed; the arrival is one of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Wait until every cp.async this thread has issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define TF_VERSION 1
+#define TF_VERSION 2
 
 #define TF_OK 0
 #define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */
@@ -68,14 +68,18 @@ const char* tf_status_string(int status);
  * packed into the weight tiles and the matrix is reordered so that each
  * consumer's tiles are contiguous, valid up to 32K).
  *
- * Blob = 64-byte header + NB*KT tiles (NB = ceil(N/128), KT = ceil(K/128)),
- * tile (nb, kt) at byte 64 + (nb*KT + kt) * tile_bytes.  A tile holds a
- * 128 x 128 block of codes in mma.sync fragment order, then its BF16 scales,
- * then its zeros, so one contiguous read brings everything the tile needs.
- * The header is little-endian: u32 magic 0x4B504654, u32 version 1, i32 N,
- * K, bits, group, tile_n (128), tile_k (128), NB, KT, tile_bytes,
- * groups_per_tile, u64 total_bytes, 8 zero bytes.  Padding rows (n >= N)
- * and columns (k >= K) dequantise to exactly zero.
+ * Blob = 64-byte header + S*KT units (S = 8*ceil(N/128) slabs of 16 rows,
+ * KT = ceil(K/128)).  Unit (s, kt) covers rows 16s..16s+15 and columns
+ * 128kt..128kt+127 of W and sits at byte 64 + (s*KT + kt) * unit_bytes:
+ * slab-major, so the units of any run of whole slabs are one contiguous
+ * range, and the eight slabs 8nb..8nb+7 at one kt form a 128 x 128 tile.
+ * A unit holds its 16 x 128 codes in mma.sync fragment order, then its BF16
+ * scales, then its zeros, then zero padding to a multiple of 16 bytes, so one
+ * contiguous read brings everything the unit needs.  The header is
+ * little-endian: u32 magic 0x4B504654, u32 version 2, i32 N, K, bits, group,
+ * unit_n (16), unit_k (128), S, KT, unit_bytes, groups_per_unit,
+ * u64 total_bytes, 8 zero bytes.  Padding rows (n >= N) and columns (k >= K)
+ * dequantise to exactly zero.
  */
 
 /* Size in bytes of the blob for this layer; writes *bytes. */

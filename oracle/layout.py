@@ -9,41 +9,43 @@ fix two properties of the offline layout: (a) the quantisation metadata
 (scales and zero points) is packed *into* the weight tiles, so that everything
 a tile needs for its dequantisation is contiguous, and (b) the matrix is
 reordered so that the tiles one consumer streams are contiguous, which removes
-large strides and keeps the layout valid for dimensions up to 32K.  The tile
+large strides and keeps the layout valid for dimensions up to 32K.  The unit
 shape and element order below are this implementation's GB300 design (the
 pages' AIE tile shapes are prior art):
 
-Blob = 64-byte header, then ``NB * KT`` tiles of ``tile_bytes`` each; tile
-``(nb, kt)`` sits at byte ``64 + (nb * KT + kt) * tile_bytes`` (n-block major:
-the K tiles of one 128-row block are contiguous).  ``NB = ceil(N / 128)``,
-``KT = ceil(K / 128)``.
+Blob = 64-byte header, then ``S * KT`` units of ``unit_bytes`` each.  A unit
+covers one 16-row slab of W (rows ``16 s .. 16 s + 15``) and 128 columns of K
+(``128 kt .. 128 kt + 127``).  Unit ``(s, kt)`` sits at byte
+``64 + (s * KT + kt) * unit_bytes``: slab-major, so all K units of a slab —
+and of any run of whole slabs — are contiguous.  ``S = 8 * ceil(N / 128)``
+(rows padded to a multiple of 128, so that eight consecutive slabs form a
+128-row tile), ``KT = ceil(K / 128)``.
 
-Header (little-endian): u32 magic 0x4B504654 ('TFPK'), u32 version 1,
-i32 N, i32 K, i32 bits, i32 group (0 = per channel), i32 tile_n 128,
-i32 tile_k 128, i32 NB, i32 KT, i32 tile_bytes, i32 groups_per_tile,
+Header (little-endian): u32 magic 0x4B504654 ('TFPK'), u32 version 2,
+i32 N, i32 K, i32 bits, i32 group (0 = per channel), i32 unit_n 16,
+i32 unit_k 128, i32 S, i32 KT, i32 unit_bytes, i32 groups_per_unit,
 u64 total_bytes, 8 zero bytes.
 
-Tile = weights (128 * 128 * bits / 8 bytes), then scales, then zeros.
+Unit = codes (16 * 128 * bits / 8 bytes), then scales, then zeros, then zero
+padding to a multiple of 16 bytes.
 
-Weights: 8 row blocks ``mb`` of 16 rows x 2 K-quads ``h`` of 64 columns; block
-``(mb, h)`` starts at byte ``(mb * 2 + h) * 32 * P`` with ``P = 16`` (INT4) or
-32 (INT8) bytes per slot.  Slot ``p = 4 gr + t`` (``gr`` in 0..7, ``t`` in
-0..3: the lane order of an mma.sync fragment) holds four words ``j = 0..3``;
-word j holds eight codes ``i = 0..7``: INT4 code i sits at bits ``4 i`` of the
-little-endian uint32 at slot byte ``4 j``; INT8 code i is slot byte
-``8 j + i``.  With ``r = i & 3`` and
-``e = i >> 2``, code i of word j in slot (gr, t) is the weight at tile
-row / column::
+Codes: 2 K-halves ``h`` of 64 columns; half h starts at byte ``h * 32 * P``
+with ``P = 16`` (INT4) or 32 (INT8) bytes per slot.  Slot ``p = 4 gr + t``
+(``gr`` in 0..7, ``t`` in 0..3: the lane order of an mma.sync fragment) holds
+four words ``j = 0..3``; word j holds eight codes ``i = 0..7``: INT4 code i
+sits at bits ``4 i`` of the little-endian uint32 at slot byte ``4 j``; INT8
+code i is slot byte ``8 j + i``.  With ``r = i & 3`` and ``e = i >> 2``, code
+i of word j in slot (gr, t) is the weight at unit row / column::
 
-    row = mb * 16 + gr + 8 * (r & 1)
+    row = gr + 8 * (r & 1)
     col = h * 64 + 16 * t + 4 * j + 2 * (r >> 1) + e
 
-Scales: bf16 ``[gi][mb][gr][e]`` (``256 * GPT`` bytes) = scale of row
-``mb*16 + gr + 8e`` in the group of tile column block ``gi``.  Zeros: INT4 one
-byte per ``[gi][mb][gr]`` (low nibble row ``gr``, high nibble row ``gr + 8``);
-INT8 one byte per ``[gi][mb][gr][e]``.  ``GPT`` (groups per tile) is
-``128 / g`` for g in {32, 64}, else 1; column block gi covers tile columns
-``[gi * g, (gi + 1) * g)`` (all 128 when GPT = 1, whose group is
+Scales: bf16 ``[gi][gr][e]`` (``32 * GPU`` bytes) = scale of unit row
+``gr + 8e`` in the group of unit column block ``gi``.  Zeros: INT4 one byte per
+``[gi][gr]`` (low nibble row ``gr``, high nibble row ``gr + 8``; 8 bytes per
+gi); INT8 one byte per ``[gi][gr][e]`` (16 bytes per gi).  ``GPU`` (groups per
+unit) is ``128 / g`` for g in {32, 64}, else 1; column block gi covers unit
+columns ``[gi * g, (gi + 1) * g)`` (all 128 when GPU = 1, whose group is
 ``kt * 128 // g``).
 
 Padding: rows >= N have q = z = 0 and s = 0; columns >= K hold q = z of their
@@ -57,56 +59,56 @@ import struct
 import numpy as np
 
 MAGIC = 0x4B504654
-VERSION = 1
+VERSION = 2
 HEADER_BYTES = 64
-TILE_N = 128
-TILE_K = 128
+UNIT_N = 16
+UNIT_K = 128
+TILE_N = 128  # rows per 128-row block; S = 8 * ceil(N / 128)
 _HDR = "<IIiiiiiiiiiiQ"
 
 
-def groups_per_tile(group: int) -> int:
-    return TILE_K // group if group in (32, 64) else 1
+def groups_per_unit(group: int) -> int:
+    return UNIT_K // group if group in (32, 64) else 1
 
 
-def tile_bytes(bits: int, group: int) -> int:
-    gpt = groups_per_tile(group)
-    w = TILE_N * TILE_K * bits // 8
-    s = 2 * TILE_N * gpt
-    z = (TILE_N // 2 if bits == 4 else TILE_N) * gpt
-    return (w + s + z + 15) // 16 * 16
+def unit_bytes(bits: int, group: int) -> int:
+    gpu = groups_per_unit(group)
+    codes = UNIT_N * UNIT_K * bits // 8
+    scales = 2 * UNIT_N * gpu
+    zeros = (UNIT_N // 2 if bits == 4 else UNIT_N) * gpu
+    return (codes + scales + zeros + 15) // 16 * 16
 
 
 def blob_geometry(N: int, K: int, bits: int, group: int):
-    nb = -(-N // TILE_N)
-    kt = -(-K // TILE_K)
-    tb = tile_bytes(bits, group)
-    return nb, kt, tb, HEADER_BYTES + nb * kt * tb
+    """(S, KT, unit_bytes, total_bytes)."""
+    s = 8 * -(-N // TILE_N)
+    kt = -(-K // UNIT_K)
+    ub = unit_bytes(bits, group)
+    return s, kt, ub, HEADER_BYTES + s * kt * ub
 
 
 def header(N, K, bits, group) -> bytes:
-    nb, kt, tb, total = blob_geometry(N, K, bits, group)
-    h = struct.pack(_HDR, MAGIC, VERSION, N, K, bits, group, TILE_N, TILE_K,
-                    nb, kt, tb, groups_per_tile(group), total)
+    s, kt, ub, total = blob_geometry(N, K, bits, group)
+    h = struct.pack(_HDR, MAGIC, VERSION, N, K, bits, group, UNIT_N, UNIT_K,
+                    s, kt, ub, groups_per_unit(group), total)
     return h + bytes(HEADER_BYTES - len(h))
 
 
 def code_coordinates():
-    """Tile (row, col) of every code of a tile, in blob order (mb, h, p, j, i)."""
-    mb, h, p, j, i = np.meshgrid(np.arange(8), np.arange(2), np.arange(32), np.arange(4),
-                                 np.arange(8), indexing="ij")
+    """Unit (row, col) of every code of a unit, in blob order (h, p, j, i)."""
+    h, p, j, i = np.meshgrid(np.arange(2), np.arange(32), np.arange(4), np.arange(8), indexing="ij")
     gr = p // 4
     t = p % 4
     r = i & 3
     e = i >> 2
-    row = mb * 16 + gr + 8 * (r & 1)
+    row = gr + 8 * (r & 1)
     col = h * 64 + 16 * t + 4 * j + 2 * (r >> 1) + e
     return row.ravel(), col.ravel()
 
 
 def _meta_rows():
-    """Tile rows of the metadata entries, shape [mb][gr][e]."""
-    return (np.arange(8)[:, None, None] * 16 + np.arange(8)[None, :, None]
-            + 8 * np.arange(2)[None, None, :])
+    """Unit rows of the metadata entries, shape [gr][e]."""
+    return np.arange(8)[:, None] + 8 * np.arange(2)[None, :]
 
 
 def prepack(qweight, scales_bits, zeros, N, K, bits, group) -> np.ndarray:
@@ -115,13 +117,13 @@ def prepack(qweight, scales_bits, zeros, N, K, bits, group) -> np.ndarray:
 
     q = unpack(qweight, bits, K)
     g = K if group == 0 else group
-    nb, kt, tb, total = blob_geometry(N, K, bits, group)
-    gpt = groups_per_tile(group)
-    Np, Kp = nb * TILE_N, kt * TILE_K
+    S, KT, ub, total = blob_geometry(N, K, bits, group)
+    gpu = groups_per_unit(group)
+    Np, Kp = S * UNIT_N, KT * UNIT_K
     n_groups = K // g
     col = np.arange(Kp)
     # group of every padded column (may point past the last group in the K pad)
-    gidx = col // g if gpt > 1 else (col // TILE_K * TILE_K) // g
+    gidx = col // g if gpu > 1 else (col // UNIT_K * UNIT_K) // g
     width = max(n_groups, int(gidx.max()) + 1)
     s_pad = np.zeros((Np, width), dtype=np.uint16)
     z_pad = np.zeros((Np, width), dtype=np.uint8)
@@ -134,38 +136,38 @@ def prepack(qweight, scales_bits, zeros, N, K, bits, group) -> np.ndarray:
 
     out = np.zeros(total, dtype=np.uint8)
     out[:HEADER_BYTES] = np.frombuffer(header(N, K, bits, group), dtype=np.uint8)
-    row, colt = code_coordinates()
+    row, colu = code_coordinates()
     mrows = _meta_rows()
-    wbytes = TILE_N * TILE_K * bits // 8
-    zb = (TILE_N // 2) if bits == 4 else TILE_N
-    for b in range(nb):
-        for t in range(kt):
-            base = HEADER_BYTES + (b * kt + t) * tb
-            codes = q_pad[b * TILE_N + row, t * TILE_K + colt]
+    cbytes = UNIT_N * UNIT_K * bits // 8
+    zb = (UNIT_N // 2) if bits == 4 else UNIT_N
+    for s in range(S):
+        for t in range(KT):
+            base = HEADER_BYTES + (s * KT + t) * ub
+            codes = q_pad[s * UNIT_N + row, t * UNIT_K + colu]
             if bits == 4:
                 c = codes.reshape(-1, 8).astype(np.uint32)
                 words = np.zeros(c.shape[0], dtype=np.uint32)
                 for i in range(8):
                     words |= c[:, i] << np.uint32(4 * i)
-                out[base:base + wbytes] = words.astype("<u4").view(np.uint8)
+                out[base:base + cbytes] = words.astype("<u4").view(np.uint8)
             else:
-                out[base:base + wbytes] = codes
-            sptr = base + wbytes
-            zptr = sptr + 256 * gpt
-            for gi in range(gpt):
-                grp = gidx[t * TILE_K + gi * (g if gpt > 1 else 0)]
-                s = s_pad[b * TILE_N + mrows, grp]
-                z = z_pad[b * TILE_N + mrows, grp]
-                out[sptr + gi * 256: sptr + (gi + 1) * 256] = s.astype("<u2").view(np.uint8).ravel()
-                zz = (z[..., 0] | (z[..., 1] << 4)).astype(np.uint8).ravel() if bits == 4 else z.ravel()
+                out[base:base + cbytes] = codes
+            sptr = base + cbytes
+            zptr = sptr + 32 * gpu
+            for gi in range(gpu):
+                grp = gidx[t * UNIT_K + gi * (g if gpu > 1 else 0)]
+                sv = s_pad[s * UNIT_N + mrows, grp]
+                zv = z_pad[s * UNIT_N + mrows, grp]
+                out[sptr + gi * 32: sptr + (gi + 1) * 32] = sv.astype("<u2").view(np.uint8).ravel()
+                zz = (zv[:, 0] | (zv[:, 1] << 4)).astype(np.uint8) if bits == 4 else zv.ravel()
                 out[zptr + gi * zb: zptr + (gi + 1) * zb] = zz
     return out
 
 
 def parse_header(blob) -> dict:
     blob = np.asarray(blob, dtype=np.uint8)
-    keys = ("magic", "version", "N", "K", "bits", "group", "tile_n", "tile_k", "NB", "KT",
-            "tile_bytes", "groups_per_tile", "total_bytes")
+    keys = ("magic", "version", "N", "K", "bits", "group", "unit_n", "unit_k", "S", "KT",
+            "unit_bytes", "groups_per_unit", "total_bytes")
     return dict(zip(keys, struct.unpack(_HDR, blob[:56].tobytes())))
 
 
@@ -175,39 +177,38 @@ def unprepack(blob: np.ndarray):
     hd = parse_header(blob)
     assert hd["magic"] == MAGIC and hd["version"] == VERSION
     N, K, bits, group = hd["N"], hd["K"], hd["bits"], hd["group"]
-    nb, kt, tb, gpt = hd["NB"], hd["KT"], hd["tile_bytes"], hd["groups_per_tile"]
+    S, KT, ub, gpu = hd["S"], hd["KT"], hd["unit_bytes"], hd["groups_per_unit"]
     g = K if group == 0 else group
     n_groups = K // g
-    row, colt = code_coordinates()
+    row, colu = code_coordinates()
     mrows = _meta_rows()
-    wbytes = TILE_N * TILE_K * bits // 8
-    zb = (TILE_N // 2) if bits == 4 else TILE_N
-    q = np.zeros((nb * TILE_N, kt * TILE_K), dtype=np.uint8)
-    scales = np.zeros((nb * TILE_N, n_groups), dtype=np.uint16)
-    zeros = np.zeros((nb * TILE_N, n_groups), dtype=np.uint8)
-    for b in range(nb):
-        for t in range(kt):
-            base = HEADER_BYTES + (b * kt + t) * tb
+    cbytes = UNIT_N * UNIT_K * bits // 8
+    zb = (UNIT_N // 2) if bits == 4 else UNIT_N
+    q = np.zeros((S * UNIT_N, KT * UNIT_K), dtype=np.uint8)
+    scales = np.zeros((S * UNIT_N, n_groups), dtype=np.uint16)
+    zeros = np.zeros((S * UNIT_N, n_groups), dtype=np.uint8)
+    for s in range(S):
+        for t in range(KT):
+            base = HEADER_BYTES + (s * KT + t) * ub
             if bits == 4:
-                words = blob[base:base + wbytes].view("<u4")
+                words = blob[base:base + cbytes].view("<u4")
                 codes = (words[:, None] >> (4 * np.arange(8, dtype=np.uint32))[None, :]) & 0xF
                 codes = codes.astype(np.uint8).ravel()
             else:
-                codes = blob[base:base + wbytes]
-            q[b * TILE_N + row, t * TILE_K + colt] = codes
-            sptr = base + wbytes
-            zptr = sptr + 256 * gpt
-            for gi in range(gpt):
-                c0 = t * TILE_K + gi * (g if gpt > 1 else 0)
+                codes = blob[base:base + cbytes]
+            q[s * UNIT_N + row, t * UNIT_K + colu] = codes
+            sptr = base + cbytes
+            zptr = sptr + 32 * gpu
+            for gi in range(gpu):
+                c0 = t * UNIT_K + gi * (g if gpu > 1 else 0)
                 if c0 >= K:
                     continue
                 grp = c0 // g
-                s = blob[sptr + gi * 256: sptr + (gi + 1) * 256].view("<u2").reshape(8, 8, 2)
+                sv = blob[sptr + gi * 32: sptr + (gi + 1) * 32].view("<u2").reshape(8, 2)
                 zz = blob[zptr + gi * zb: zptr + (gi + 1) * zb]
-                z = np.stack([zz & 0xF, zz >> 4], axis=-1).reshape(8, 8, 2) if bits == 4 \
-                    else zz.reshape(8, 8, 2)
-                scales[b * TILE_N + mrows, grp] = s
-                zeros[b * TILE_N + mrows, grp] = z
+                zv = np.stack([zz & 0xF, zz >> 4], axis=-1) if bits == 4 else zz.reshape(8, 2)
+                scales[s * UNIT_N + mrows, grp] = sv
+                zeros[s * UNIT_N + mrows, grp] = zv
     q = q[:N, :K]
     if bits == 4:
         qr = q.reshape(N, K // 8, 8).astype(np.uint32)

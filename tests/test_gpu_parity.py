@@ -57,8 +57,44 @@ def test_gemv_small(N, K, bits, group, M):
     check_close(y, ref, f"gemv {N}x{K} w{bits} g{group} M={M}")
 
 
-def test_gemv_deterministic_and_workspace_reusable():
+# Layers with at least one 16-row slab per SM (and K >= 1024) take the slab
+# GEMV: whole slabs per CTA, K split over the CTA's warps, no workspace.
+SLAB_FORMATS = [
+    (2440, 1016, 4, 0), (2440, 1152, 4, 128), (4104, 2048, 4, 32), (2432, 4096, 4, 64),
+    (3000, 2048, 8, 0), (2560, 1280, 8, 64), (2448, 1024, 8, 32), (5000, 3072, 4, 128),
+]
+
+
+def _sms():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("N,K,bits,group", SLAB_FORMATS)
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_gemv_slab(N, K, bits, group, M):
+    assert -(-N // 16) >= _sms() and -(-K // 128) >= 8, "shape meant for the slab GEMV"
+    if not (M == 8 and bits == 4 and group in (32, 64)):  # those stages do not fit twice per SM: tile GEMV
+        assert tf.gemv_workspace_size(N, K, bits, group, M) == 0
+    qw, W = layer(N, K, bits, group, 23)
+    xb = synth.make_activations(M, K, 23)
+    y = to_host_bits(tf.gemv(W, to_dev_bf16(xb)))
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
+    check_close(y, ref, f"slab gemv {N}x{K} w{bits} g{group} M={M}")
+
+
+def test_gemv_slab_deterministic():
     N, K = 4096, 11008
+    qw, W = layer(N, K, 4, 128, 4)
+    x = to_dev_bf16(synth.make_activations(1, K, 4))
+    a = to_host_bits(tf.gemv(W, x))
+    for _ in range(3):
+        np.testing.assert_array_equal(a, to_host_bits(tf.gemv(W, x)))
+
+
+def test_gemv_deterministic_and_workspace_reusable():
+    """Tile GEMV with K split over many CTAs (1024 rows: fewer slabs than SMs)."""
+    N, K = 1024, 11008
     qw, W = layer(N, K, 4, 128, 4)
     x = to_dev_bf16(synth.make_activations(1, K, 4))
     a = to_host_bits(tf.gemv(W, x))
@@ -68,7 +104,8 @@ def test_gemv_deterministic_and_workspace_reusable():
     # the workspace is handed back zero-filled (counters reset)
     ws = W.workspace(1)
     import torch
-    n_counter = 4096 // 128 * 8
+    assert ws.numel() > 16
+    n_counter = N // 128 * 8
     assert int(ws.view(torch.int32)[-((n_counter + 63) // 64 * 64):].abs().sum()) == 0
 
 

@@ -3,8 +3,8 @@
 The pages fix that the pre-tiling is a pure reordering with the metadata
 co-located in each tile (TileFuse, Methodology 2 "Interleaved pre-tiling"),
 valid up to 32K.  So: every weight lands on exactly one (byte, nibble), the
-round trip is the identity, each tile's metadata follows its weights, and the
-padding dequantises to zero.
+round trip is the identity, each unit's metadata follows its weights, the
+units of one slab are contiguous, and the padding dequantises to zero.
 """
 
 import numpy as np
@@ -15,11 +15,11 @@ from oracle import layout as L
 from oracle import tf_oracle as O
 
 
-def test_code_coordinates_are_a_bijection_of_the_tile():
+def test_code_coordinates_are_a_bijection_of_the_unit():
     row, col = L.code_coordinates()
-    assert row.size == L.TILE_N * L.TILE_K
-    flat = row * L.TILE_K + col
-    assert np.array_equal(np.sort(flat), np.arange(L.TILE_N * L.TILE_K))
+    assert row.size == L.UNIT_N * L.UNIT_K
+    flat = row * L.UNIT_K + col
+    assert np.array_equal(np.sort(flat), np.arange(L.UNIT_N * L.UNIT_K))
 
 
 def test_fragment_slots_follow_mma_register_order():
@@ -60,31 +60,53 @@ def test_every_weight_lands_on_a_distinct_nibble():
     s = np.full((N, K // 64), 0x3F80, np.uint16)
     z = np.zeros((N, K // 64), np.uint8)
     blob = L.prepack(qweight, s, z, N, K, 4, 64)
-    nb, kt, tb, total = L.blob_geometry(N, K, 4, 64)
+    S, kt, ub, total = L.blob_geometry(N, K, 4, 64)
     row, col = L.code_coordinates()
-    seen = np.zeros((nb * 128, kt * 128), np.int32)
-    for b in range(nb):
+    seen = np.zeros((S * 16, kt * 128), np.int32)
+    for sl in range(S):
         for t in range(kt):
-            seen[b * 128 + row, t * 128 + col] += 1
+            seen[sl * 16 + row, t * 128 + col] += 1
     assert (seen == 1).all()
     np.testing.assert_array_equal(O.unpack_w4(L.unprepack(blob)[0], K), q)
 
 
-def test_metadata_is_contiguous_with_its_tile():
+def test_metadata_is_contiguous_with_its_unit():
     N, K, bits, group = 128, 256, 4, 64
     qw = synth.make_weights(N, K, bits, group, 2)
     blob = L.prepack(qw.qweight, qw.scales, qw.zeros, N, K, bits, group)
-    nb, kt, tb, _ = L.blob_geometry(N, K, bits, group)
-    assert tb == 8192 + 512 + 128
-    for t in range(kt):
-        base = L.HEADER_BYTES + t * tb
-        s = blob[base + 8192: base + 8192 + 512].view("<u2").reshape(2, 8, 8, 2)
-        # [gi][mb][gr][e] -> scale of row mb*16 + gr + 8e, group 2t + gi
-        for gi in range(2):
-            for mb in (0, 7):
-                for gr in (0, 5):
+    S, kt, ub, _ = L.blob_geometry(N, K, bits, group)
+    assert ub == 1024 + 64 + 16
+    for sl in (0, 3, 7):
+        for t in range(kt):
+            base = L.HEADER_BYTES + (sl * kt + t) * ub
+            s = blob[base + 1024: base + 1024 + 64].view("<u2").reshape(2, 8, 2)
+            z = blob[base + 1088: base + 1104].reshape(2, 8)
+            # [gi][gr][e] -> row 16 sl + gr + 8e, group 2t + gi
+            for gi in range(2):
+                for gr in (0, 5, 7):
                     for e in (0, 1):
-                        assert s[gi, mb, gr, e] == qw.scales[mb * 16 + gr + 8 * e, 2 * t + gi]
+                        n = sl * 16 + gr + 8 * e
+                        assert s[gi, gr, e] == qw.scales[n, 2 * t + gi]
+                        assert (z[gi, gr] >> (4 * e)) & 0xF == qw.zeros[n, 2 * t + gi]
+
+
+def test_slab_units_are_contiguous():
+    """Unit (s, kt + 1) follows unit (s, kt); slab s + 1 follows the last unit of slab s."""
+    N, K = 48, 384
+    q = np.zeros((N, K), np.uint8)
+    q[np.arange(N), (np.arange(N) * 7) % K] = 1 + np.arange(N) % 15  # one tagged code per row
+    blob = L.prepack(synth.pack_w4(q), np.full((N, 3), 0x3F80, np.uint16), np.zeros((N, 3), np.uint8),
+                     N, K, 4, 128)
+    S, kt, ub, total = L.blob_geometry(N, K, 4, 128)
+    assert (S, kt, ub) == (8, 3, 1072) and total == 64 + 8 * 3 * 1072
+    row, col = L.code_coordinates()
+    for n in range(N):
+        k = (n * 7) % K
+        sl, t = n // 16, k // 128
+        base = L.HEADER_BYTES + (sl * kt + t) * ub
+        idx = np.flatnonzero((row == n % 16) & (col == k % 128))[0]
+        word = int(blob[base + 4 * (idx // 8): base + 4 * (idx // 8) + 4].view("<u4")[0])
+        assert (word >> (4 * (idx % 8))) & 0xF == q[n, k]
 
 
 def test_padding_dequantises_to_zero():
@@ -92,29 +114,31 @@ def test_padding_dequantises_to_zero():
     N, K = 130, 200
     qw = synth.make_weights(N, K, 8, 0, 4)
     blob = L.prepack(qw.qweight, qw.scales, qw.zeros, N, K, 8, 0)
-    nb, kt, tb, _ = L.blob_geometry(N, K, 8, 0)
+    S, kt, ub, _ = L.blob_geometry(N, K, 8, 0)
+    assert (S, kt, ub) == (16, 2, 2096)
     row, col = L.code_coordinates()
-    for b in range(nb):
+    for sl in range(S):
         for t in range(kt):
-            base = L.HEADER_BYTES + (b * kt + t) * tb
-            codes = blob[base: base + 16384]
-            sv = blob[base + 16384: base + 16384 + 256].view("<u2").reshape(8, 8, 2)
-            zv = blob[base + 16384 + 256: base + 16384 + 384].reshape(8, 8, 2)
-            n = b * 128 + row
+            base = L.HEADER_BYTES + (sl * kt + t) * ub
+            codes = blob[base: base + 2048]
+            sv = blob[base + 2048: base + 2080].view("<u2").reshape(8, 2)
+            zv = blob[base + 2080: base + 2096].reshape(8, 2)
+            n = sl * 16 + row
             k = t * 128 + col
-            mbk, grk, ek = row // 16, row % 8, (row % 16) // 8
-            w = (codes.astype(np.int64) - zv[mbk, grk, ek]) * sv[mbk, grk, ek].astype(np.int64)
+            grk, ek = row % 8, row // 8
+            w = (codes.astype(np.int64) - zv[grk, ek]) * sv[grk, ek].astype(np.int64)
             pad = (n >= N) | (k >= K)
             assert (w[pad] == 0).all()
 
 
-def test_tile_sizes_are_16_byte_multiples():
+def test_unit_sizes_are_16_byte_multiples():
     for bits in (4, 8):
         for group in (32, 64, 128, 0, 256):
-            assert L.tile_bytes(bits, group) % 16 == 0
-    assert L.tile_bytes(4, 128) == 8512 and L.tile_bytes(8, 0) == 16768
+            assert L.unit_bytes(bits, group) % 16 == 0
+    assert L.unit_bytes(4, 128) == 1072 and L.unit_bytes(8, 0) == 2096
+    assert L.unit_bytes(4, 32) == 1024 + 4 * 40 and L.unit_bytes(8, 64) == 2048 + 2 * 48
 
 
 def test_32k_geometry():
-    nb, kt, tb, total = L.blob_geometry(32768, 32768, 4, 128)
-    assert (nb, kt) == (256, 256) and total == 64 + 65536 * 8512
+    S, kt, ub, total = L.blob_geometry(32768, 32768, 4, 128)
+    assert (S, kt) == (2048, 256) and total == 64 + 2048 * 256 * 1072

@@ -46,7 +46,8 @@ def _noalloc(W, x, y):
 
 
 @pytest.mark.parametrize("N,K,bits,group,M", [
-    (4096, 4096, 4, 128, 1),      # a decode projection: every row block is split over several CTAs
+    (4096, 4096, 4, 128, 1),      # a decode projection (slab GEMV: no scratch needed)
+    (1024, 11008, 4, 128, 1),     # few rows, long K: every row block is split over many CTAs
     (1000, 1016, 8, 0, 3),        # ragged N and K, INT8 per channel, several tokens
     (8192, 32768, 4, 128, 1),     # long K
     (256, 512, 4, 128, 8),
