@@ -4,9 +4,9 @@
 // *once* into on-chip memory and the BF16 result is reused for the tile's
 // matrix operations.  Here, per CTA output tile of 128 weight rows x BN
 // tokens (BN <= 256):
-//   warp 0       streams pre-tiled weight tiles (eight 1-D bulk copies, one
-//                per 16-row unit, each carrying its own scales and zeros)
-//                and the matching activation slabs (2-D TMA, 128-byte
+//   warp 0       streams pre-tiled weight tiles (one 3-D TMA box: the eight
+//                16-row units of the tile, each carrying its own scales and
+//                zeros) and the matching activation slabs (2-D TMA, 128-byte
 //                swizzle) into shared-memory rings;
 //   warps 6..21  unpack + dequantise one (16-row block, 64-column slab) of
 //                each tile into the UMMA K-major 128-byte-swizzled layout
@@ -80,6 +80,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int P, int OPS) {
 
 template <int BITS, int GPT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                           const __grid_constant__ CUtensorMap tmw,
                                                            const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     mbar_init(B.drain, 1);
     mbar_init_fence();
     prefetch_tensormap(&tmx);
+    prefetch_tensormap(&tmw);
   }
   if (warp == 1) {
     tmem_alloc(B.tmem_slot, kTmemCols);
@@ -118,33 +120,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    // Lane i < 8 copies unit i (rows 16i .. 16i + 15) of each tile; lane 0
-    // arms the barriers and loads the activation slabs.
-    constexpr int UB = unit_bytes_gpu(BITS, GPT);
-    int ps = 0, os = 0;
-    uint32_t pph = 0, oph = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-      const int nb = tile / a.MT, mt = tile - nb * a.MT;
-      const uint8_t* src = a.units + ((size_t)(nb * kSlabsPerTile + (lane & 7)) * a.KT) * UB;
-      for (int kt = 0; kt < a.KT && ok; ++kt) {
-        ok = mbar_wait_warp(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
-        __syncwarp();
-        if (lane < kSlabsPerTile)
-          bulk_load(sbase + (uint32_t)(ps * a.tile_bytes + lane * UB), src + (size_t)kt * UB, (uint32_t)UB,
-                    B.full_p + 8 * ps);
-        if (++ps == a.P) { ps = 0; pph ^= 1; }
-        for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait_warp(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
+    if (lane == 0) {
+      int ps = 0, os = 0;
+      uint32_t pph = 0, oph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+        const int nb = tile / a.MT, mt = tile - nb * a.MT;
+        for (int kt = 0; kt < a.KT && ok; ++kt) {
+          ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
           if (!ok) break;
-          if (lane == 0) {
+          mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
+          const uint32_t dst = sbase + (uint32_t)(ps * a.tile_bytes);
+          if (BITS == 4)
+            tma_load_3d(dst, &tmw, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
+          else
+            tma_load_4d(dst, &tmw, 0, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
+          if (++ps == a.P) { ps = 0; pph ^= 1; }
+          for (int h = 0; h < 2; ++h) {
+            ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
+            if (!ok) break;
             mbar_arrive_expect_tx(B.full_op + 8 * os, x_slab_bytes);
             tma_load_2d(sbase + a.off_op + (uint32_t)os * op_stage_bytes + kSlabBytesW, &tmx,
                         kt * kTileK + h * 64, mt * a.BN, B.full_op + 8 * os);
+            if (++os == a.OPS) { os = 0; oph ^= 1; }
           }
-          if (++os == a.OPS) { os = 0; oph ^= 1; }
         }
       }
     }
@@ -343,7 +342,7 @@ int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
 }
 
 template <int BITS, int GPT>
-int launch_gemm(const CUtensorMap& map, const GemmPlan& P, cudaStream_t s) {
+int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const GemmPlan& P, cudaStream_t s) {
   auto kfn = gemm_kernel<BITS, GPT>;
   // Opt in once per device to the largest shared-memory carve-out.
   static std::atomic<unsigned long long> opted{0};
@@ -354,7 +353,7 @@ int launch_gemm(const CUtensorMap& map, const GemmPlan& P, cudaStream_t s) {
       return TF_ERR_CUDA;
     opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }
-  kfn<<<P.grid, kThreads, P.smem, s>>>(map, P.a);
+  kfn<<<P.grid, kThreads, P.smem, s>>>(map, wmap, P.a);
   return launch_status();
 }
 
@@ -379,17 +378,19 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   P.a.y = y;
   P.a.err = device_error_ptr();
   if (!P.a.err) return TF_ERR_CUDA;
-  CUtensorMap map;
+  CUtensorMap map, wmap;
   rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
   if (rc) return rc;
+  rc = encode_units_map(P.a.units, G.S, G.KT, G.unit_bytes, &wmap);
+  if (rc) return rc;
   if (bits == 4) {
-    if (G.gpt == 1) return launch_gemm<4, 1>(map, P, stream);
-    if (G.gpt == 2) return launch_gemm<4, 2>(map, P, stream);
-    return launch_gemm<4, 4>(map, P, stream);
+    if (G.gpt == 1) return launch_gemm<4, 1>(map, wmap, P, stream);
+    if (G.gpt == 2) return launch_gemm<4, 2>(map, wmap, P, stream);
+    return launch_gemm<4, 4>(map, wmap, P, stream);
   }
-  if (G.gpt == 1) return launch_gemm<8, 1>(map, P, stream);
-  if (G.gpt == 2) return launch_gemm<8, 2>(map, P, stream);
-  return launch_gemm<8, 4>(map, P, stream);
+  if (G.gpt == 1) return launch_gemm<8, 1>(map, wmap, P, stream);
+  if (G.gpt == 2) return launch_gemm<8, 2>(map, wmap, P, stream);
+  return launch_gemm<8, 4>(map, wmap, P, stream);
 }
 
 }  // extern "C"

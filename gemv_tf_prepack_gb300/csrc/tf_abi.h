@@ -22,6 +22,13 @@ unsigned* device_error_ptr();
 int encode_x_map(const uint16_t* x, int M, int K, CUtensorMap* map);
 int encode_x_map_sw128(const uint16_t* x, int M, int K, int rows, CUtensorMap* map);
 
+// TMA map over the S x KT units of a blob (8-byte elements): one box is the
+// eight units of a 128-row tile at one kt, written densely (unit after unit)
+// to shared memory.  INT4 units: dims {unit/8, KT, S}, box {unit/8, 1, 8};
+// INT8 units (more than 256 elements): dims {unit/16, 2, KT, S}, box
+// {unit/16, 2, 1, 8}.
+int encode_units_map(const uint8_t* units, int S, int KT, int unit_bytes, CUtensorMap* map);
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Streaming multiprocessors of the current device (cached per device).

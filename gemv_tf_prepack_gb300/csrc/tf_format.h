@@ -54,9 +54,12 @@ constexpr int kUnitScaleBytes = 2 * kSlabN;
 TF_HD int unit_zero_bytes(int bits) { return bits == 4 ? kSlabN / 2 : kSlabN; }
 
 // Unit size for a given number of groups per unit (a compile-time constant
-// of every kernel instantiation).
+// of every kernel instantiation): padded to a multiple of 16 bytes (INT4) or
+// 32 bytes (INT8, so that each half of a unit is a multiple of 16 bytes and
+// a TMA box of one half fits the 256-element limit of 8-byte elements).
 TF_HDC int unit_bytes_gpu(int bits, int gpu) {
-  return (kSlabN * kTileK * bits / 8 + (kUnitScaleBytes + (bits == 4 ? kSlabN / 2 : kSlabN)) * gpu + 15) / 16 * 16;
+  return (kSlabN * kTileK * bits / 8 + (kUnitScaleBytes + (bits == 4 ? kSlabN / 2 : kSlabN)) * gpu +
+          (bits == 4 ? 15 : 31)) / (bits == 4 ? 16 : 32) * (bits == 4 ? 16 : 32);
 }
 
 TF_HD int unit_bytes(int bits, int group) { return unit_bytes_gpu(bits, groups_per_unit(group)); }

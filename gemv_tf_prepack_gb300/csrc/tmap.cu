@@ -1,6 +1,7 @@
 // Host-side encoding of the TMA tensor maps over the activations x [M, K]
-// (BF16, row-major).  The driver entry point is resolved once through the
-// runtime, so libtf needs no link-time dependency on libcuda.
+// (BF16, row-major) and over the units of a blob.  The driver entry point is
+// resolved once through the runtime, so libtf needs no link-time dependency
+// on libcuda.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -49,6 +50,33 @@ int encode_x_map(const uint16_t* x, int M, int K, CUtensorMap* map) {
 
 int encode_x_map_sw128(const uint16_t* x, int M, int K, int rows, CUtensorMap* map) {
   return encode(x, M, K, 64, (unsigned)rows, CU_TENSOR_MAP_SWIZZLE_128B, map);
+}
+
+int encode_units_map(const uint8_t* units, int S, int KT, int unit_bytes, CUtensorMap* map) {
+  auto enc = encode_fn();
+  if (!enc) return TF_ERR_CUDA;
+  const int e = unit_bytes / 8;  // 8-byte elements per unit
+  CUresult r;
+  if (e <= 256) {
+    const cuuint64_t dims[3] = {(cuuint64_t)e, (cuuint64_t)KT, (cuuint64_t)S};
+    const cuuint64_t strides[2] = {(cuuint64_t)unit_bytes, (cuuint64_t)KT * unit_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)e, 1, (cuuint32_t)kSlabsPerTile};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t*>(units), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // INT8 units: two halves of at most 256 elements each
+    const cuuint64_t dims[4] = {(cuuint64_t)e / 2, 2, (cuuint64_t)KT, (cuuint64_t)S};
+    const cuuint64_t strides[3] = {(cuuint64_t)unit_bytes / 2, (cuuint64_t)unit_bytes,
+                                   (cuuint64_t)KT * unit_bytes};
+    const cuuint32_t box[4] = {(cuuint32_t)e / 2, 2, 1, (cuuint32_t)kSlabsPerTile};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<uint8_t*>(units), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? TF_OK : TF_ERR_CUDA;
 }
 
 }  // namespace tf

@@ -74,7 +74,8 @@ const char* tf_status_string(int status);
  * slab-major, so the units of any run of whole slabs are one contiguous
  * range, and the eight slabs 8nb..8nb+7 at one kt form a 128 x 128 tile.
  * A unit holds its 16 x 128 codes in mma.sync fragment order, then its BF16
- * scales, then its zeros, then zero padding to a multiple of 16 bytes, so one
+ * scales, then its zeros, then zero padding to a multiple of 16 (INT4) or 32
+ * (INT8) bytes, so one
  * contiguous read brings everything the unit needs.  The header is
  * little-endian: u32 magic 0x4B504654, u32 version 2, i32 N, K, bits, group,
  * unit_n (16), unit_k (128), S, KT, unit_bytes, groups_per_unit,

@@ -27,7 +27,7 @@ i32 unit_k 128, i32 S, i32 KT, i32 unit_bytes, i32 groups_per_unit,
 u64 total_bytes, 8 zero bytes.
 
 Unit = codes (16 * 128 * bits / 8 bytes), then scales, then zeros, then zero
-padding to a multiple of 16 bytes.
+padding to a multiple of 16 bytes (INT4) or 32 bytes (INT8).
 
 Codes: 2 K-halves ``h`` of 64 columns; half h starts at byte ``h * 32 * P``
 with ``P = 16`` (INT4) or 32 (INT8) bytes per slot.  Slot ``p = 4 gr + t``
@@ -76,7 +76,8 @@ def unit_bytes(bits: int, group: int) -> int:
     codes = UNIT_N * UNIT_K * bits // 8
     scales = 2 * UNIT_N * gpu
     zeros = (UNIT_N // 2 if bits == 4 else UNIT_N) * gpu
-    return (codes + scales + zeros + 15) // 16 * 16
+    align = 16 if bits == 4 else 32
+    return (codes + scales + zeros + align - 1) // align * align
 
 
 def blob_geometry(N: int, K: int, bits: int, group: int):

@@ -65,7 +65,7 @@ def test_prepack_decode_shape_round_trip():
 
 def test_prepack_sizes():
     assert tf.prepack_size(32768, 32768, 4, 128) == 64 + 2048 * 256 * 1072
-    assert tf.prepack_size(8192, 8192, 8, 0) == 64 + 64 * 64 * 16768
+    assert tf.prepack_size(8192, 8192, 8, 0) == 64 + 512 * 64 * 2112
     assert tf.prepack_size(4096, 4096, 4, 64) == 64 + 32 * 32 * 8832
 
 

@@ -115,7 +115,7 @@ def test_padding_dequantises_to_zero():
     qw = synth.make_weights(N, K, 8, 0, 4)
     blob = L.prepack(qw.qweight, qw.scales, qw.zeros, N, K, 8, 0)
     S, kt, ub, _ = L.blob_geometry(N, K, 8, 0)
-    assert (S, kt, ub) == (16, 2, 2096)
+    assert (S, kt, ub) == (16, 2, 2112)
     row, col = L.code_coordinates()
     for sl in range(S):
         for t in range(kt):
@@ -131,12 +131,14 @@ def test_padding_dequantises_to_zero():
             assert (w[pad] == 0).all()
 
 
-def test_unit_sizes_are_16_byte_multiples():
+def test_unit_sizes_are_aligned():
     for bits in (4, 8):
         for group in (32, 64, 128, 0, 256):
             assert L.unit_bytes(bits, group) % 16 == 0
-    assert L.unit_bytes(4, 128) == 1072 and L.unit_bytes(8, 0) == 2096
+    assert L.unit_bytes(4, 128) == 1072 and L.unit_bytes(8, 0) == 2112
     assert L.unit_bytes(4, 32) == 1024 + 4 * 40 and L.unit_bytes(8, 64) == 2048 + 2 * 48
+    for group in (32, 64, 128, 0):  # INT8 halves are 16-byte multiples
+        assert L.unit_bytes(8, group) % 32 == 0
 
 
 def test_32k_geometry():
