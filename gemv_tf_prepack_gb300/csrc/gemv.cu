@@ -97,19 +97,17 @@ constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
 constexpr uint64_t kGemvDrainNs = 200000000ull;  // bounded wait for copies still in flight after an error
 constexpr unsigned kErrGemvWait = 0x600;
 
-// Registers of one unit for one lane: its weight slot in both K halves, the
-// activation fragments and the unit's scale / zero words.
+// Registers of one unit's weights for one lane: its slot in both K halves
+// and the unit's scale / zero words.
 template <int BITS, int GPT>
-struct UnitRegs {
+struct WRegs {
   uint4 w[2][BITS == 4 ? 1 : 2];
-  uint4 x[2][2];
   uint32_t sp[GPT == 1 ? 1 : 2], zp[GPT == 1 ? 1 : 2];
 };
 
 // Unit-relative byte offsets of one lane's operands.
 struct LaneOffsets {
   int w, s0, s1, z0, z1, x;
-  bool x_on;  // this lane's B-fragment column is a real token (gr < M)
 };
 
 template <int BITS, int GPT>
@@ -124,27 +122,20 @@ __device__ __forceinline__ LaneOffsets lane_offsets(int lane, int g, int M) {
   o.s1 = unit_scale_offset(BITS, gi1, gr);
   o.z0 = unit_zero_offset(BITS, GPT, gi0, gr);
   o.z1 = unit_zero_offset(BITS, GPT, gi1, gr);
-  o.x_on = gr < M;
-  o.x = (o.x_on ? gr : 0) * 256 + 32 * t;
+  // B-fragment column gr is token gr; lanes past the last token read token
+  // 0 instead (their columns of D are computed but never stored).
+  o.x = (gr < M ? gr : 0) * 256 + 32 * t;
   return o;
 }
 
-// ub: the unit in shared memory; xb: its activation slice x[0..M)[128 columns].
+// ub: the unit in shared memory.
 template <int BITS, int GPT>
-__device__ __forceinline__ void load_unit(UnitRegs<BITS, GPT>& R, const uint8_t* ub, const uint8_t* xb,
-                                          const LaneOffsets& o) {
+__device__ __forceinline__ void load_w(WRegs<BITS, GPT>& R, const uint8_t* ub, const LaneOffsets& o) {
   constexpr int SB = BITS == 4 ? 16 : 32;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
     for (int v = 0; v < SB / 16; ++v) R.w[h][v] = *reinterpret_cast<const uint4*>(ub + o.w + h * 32 * SB + v * 16);
-    // Columns of B past M only feed columns of D that are never stored: those
-    // lanes keep whatever their registers hold and skip the shared-memory read.
-    if (o.x_on) {
-      R.x[h][0] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
-      R.x[h][1] = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
-    }
-  }
   R.sp[0] = *reinterpret_cast<const uint32_t*>(ub + o.s0);
   R.zp[0] = BITS == 4 ? (uint32_t)ub[o.z0] : (uint32_t)*reinterpret_cast<const uint16_t*>(ub + o.z0);
   if (GPT > 1) {
@@ -153,43 +144,47 @@ __device__ __forceinline__ void load_unit(UnitRegs<BITS, GPT>& R, const uint8_t*
   }
 }
 
-template <int BITS, int GPT>
-__device__ __forceinline__ void clear_x(UnitRegs<BITS, GPT>& R) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int v = 0; v < 2; ++v) R.x[h][v] = make_uint4(0, 0, 0, 0);
+// B fragments of K half h: x[token][h*64 + 16t .. +16] from the unit's
+// activation slice xb = x[0..M)[128 columns] in shared memory.
+__device__ __forceinline__ void load_x(uint32_t (&xs)[8], const uint8_t* xb, const LaneOffsets& o, int h) {
+  const uint4 a = *reinterpret_cast<const uint4*>(xb + o.x + h * 128);
+  const uint4 b = *reinterpret_cast<const uint4*>(xb + o.x + h * 128 + 16);
+  xs[0] = a.x; xs[1] = a.y; xs[2] = a.z; xs[3] = a.w;
+  xs[4] = b.x; xs[5] = b.y; xs[6] = b.z; xs[7] = b.w;
 }
 
-// Unpack, dequantise (bit-exact BF16) and multiply-accumulate one unit.
+// Unpack, dequantise (bit-exact BF16) and multiply-accumulate K half h of a unit.
 template <int BITS, int GPT>
-__device__ __forceinline__ void mma_unit(const UnitRegs<BITS, GPT>& R, float (&acc)[2][4]) {
+__device__ __forceinline__ void mma_half(const WRegs<BITS, GPT>& R, int h, const uint32_t (&xs)[8],
+                                         float (&acc)[4]) {
+  const int mi = GPT == 1 ? 0 : h;
+  if (BITS == 4) {
+    const MetaW4 m = meta_w4(R.sp[mi], R.zp[mi]);
+    const uint32_t words[4] = {R.w[h][0].x, R.w[h][0].y, R.w[h][0].z, R.w[h][0].w};
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int mi = GPT == 1 ? 0 : h;
-    const uint32_t xs[8] = {R.x[h][0].x, R.x[h][0].y, R.x[h][0].z, R.x[h][0].w,
-                            R.x[h][1].x, R.x[h][1].y, R.x[h][1].z, R.x[h][1].w};
-    if (BITS == 4) {
-      const MetaW4 m = meta_w4(R.sp[mi], R.zp[mi]);
-      const uint32_t words[4] = {R.w[h][0].x, R.w[h][0].y, R.w[h][0].z, R.w[h][0].w};
+    for (int j = 0; j < 4; ++j) {
+      uint32_t af[4];
+      dequant_w4(words[j], m, af);
+      mma_16816(acc, af, xs[2 * j], xs[2 * j + 1]);
+    }
+  } else {
+    const MetaW8 m = meta_w8(R.sp[mi], R.zp[mi]);
+    const uint4 v0 = R.w[h][0], v1 = R.w[h][BITS == 4 ? 0 : 1];
+    const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t af[4];
-        dequant_w4(words[j], m, af);
-        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
-      }
-    } else {
-      const MetaW8 m = meta_w8(R.sp[mi], R.zp[mi]);
-      const uint4 v0 = R.w[h][0], v1 = R.w[h][BITS == 4 ? 0 : 1];
-      const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t af[4];
-        dequant_w8(words[2 * j], words[2 * j + 1], m, af);
-        mma_16816(acc[h], af, xs[2 * j], xs[2 * j + 1]);
-      }
+    for (int j = 0; j < 4; ++j) {
+      uint32_t af[4];
+      dequant_w8(words[2 * j], words[2 * j + 1], m, af);
+      mma_16816(acc, af, xs[2 * j], xs[2 * j + 1]);
     }
   }
+}
+
+// A whole unit with its activations already in registers (xs[h]).
+template <int BITS, int GPT>
+__device__ __forceinline__ void mma_unit(const WRegs<BITS, GPT>& R, const uint32_t (&xs)[2][8], float (&acc)[2][4]) {
+  mma_half(R, 0, xs[0], acc[0]);
+  mma_half(R, 1, xs[1], acc[1]);
 }
 
 // v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1.
@@ -420,8 +415,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   const int x_stride = a.M * 256;
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  UnitRegs<BITS, GPT> R;
-  clear_x(R);
+  WRegs<BITS, GPT> R;
+  uint32_t xs[2][8];
   Segment seg = first_segment(t0, ntile, a.KT);
   // at most two segments of a contiguous range are partial: its first and its last
   int pending0 = 0, pending1 = 0, npending = 0;
@@ -432,11 +427,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     const int i0 = f * kTilesPerStage;
     const int n = ntile - i0 < kTilesPerStage ? ntile - i0 : kTilesPerStage;
     const uint8_t* st = smem + s * a.stage_bytes;
-    const uint8_t* xs = st + a.x_off;
+    const uint8_t* xst = st + a.x_off;
 #pragma unroll
     for (int j = 0; j < kTilesPerStage; ++j) {
       if (j < n) {
-        load_unit(R, st + (j * kSlabsPerTile + warp) * UB, xs + j * x_stride, o);
+        load_w(R, st + (j * kSlabsPerTile + warp) * UB, o);
+        load_x(xs[0], xst + j * x_stride, o, 0);
+        load_x(xs[1], xst + j * x_stride, o, 1);
         if (j == n - 1) {
           // the whole stage has been read: hand it back; the last warp to do
           // so refills it
@@ -452,7 +449,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
           if (__shfl_sync(0xFFFFFFFFu, refill, 0))
             issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true, lane);
         }
-        mma_unit(R, acc);
+        mma_unit(R, xs, acc);
         if (i0 + j == seg.end) {
           const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
                               acc[0][3] + acc[1][3]};
@@ -528,7 +525,7 @@ __device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int k0, 
 // by lane 0.  Per-stage activations (x_res == 0): all 32 lanes copy 16-byte
 // chunks and each lane then arrives on the stage's barrier once its copies
 // have landed (the barrier then expects 1 + 32 arrivals per fill).
-template <int BITS, int GPT>
+template <int BITS, int GPT, bool XRES>
 __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uint32_t full, int s0, int f, int st,
                                           bool weights, bool x, int lane) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
@@ -542,13 +539,13 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
     mbar_arrive_expect_tx(bar, (uint32_t)(n * UB));
     bulk_load(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar);
   }
-  if (x && !a.x_res) {
+  if (x && !XRES) {
     copy_x(a, dst + (uint32_t)a.x_off, k0, n, lane, 32);
     cp_async_mbar_arrive_noinc(bar);
   }
 }
 
-template <int BITS, int GPT>
+template <int BITS, int GPT, bool XRES>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align128(smem_raw);
@@ -571,7 +568,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
-      mbar_init(full + 8 * i, a.x_res ? 1 : 1 + 32);
+      mbar_init(full + 8 * i, XRES ? 1 : 1 + 32);
       mbar_init(empty + 8 * i, kGemvWarps);
       released[i] = 0;
     }
@@ -587,38 +584,56 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   if (warp == 0) {
     if (lane == 0) griddep_launch_dependents();
     // static weights first, before the grid dependency resolves
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT>(a, sbase, full, s0, f, f, true, false, lane);
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f, f, true, false, lane);
   }
   // y and x may still be in use by the previous grid
   griddep_wait();
-  if (a.x_res) {
+  if (XRES) {
     copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, kGemvThreads);
     cp_async_wait_all();
     __syncthreads();
   } else if (warp == 0) {
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT>(a, sbase, full, s0, f, f, false, true, lane);
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f, f, false, true, lane);
   }
 
   const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
   const int x_unit = a.M * 256;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  UnitRegs<BITS, GPT> R[UPW];
+  // This warp's units of a stage are w, w + 8, ...: their offsets in the
+  // stage and in the stage's activation slices.
+  int woff[UPW], xoff[UPW];
 #pragma unroll
-  for (int j = 0; j < UPW; ++j) clear_x(R[j]);
+  for (int j = 0; j < UPW; ++j) {
+    woff[j] = (j * kGemvWarps + warp) * UB;
+    xoff[j] = (j * kGemvWarps + warp) * x_unit;
+  }
+  const int last_n = a.KT - (a.QPS - 1) * U;  // units in the last stage of a slab (1..U)
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  WRegs<BITS, GPT> R[UPW];
+  // Resident activations are read right before their MMAs; per-stage ones
+  // must leave the stage with the weights, before it is handed back.
+  uint32_t xs[XRES ? 1 : UPW][2][8];
   bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
-  int st = 0, q = 0, si = 0;
+  int st = 0, q = 0, si = 0, slot = 0;
+  unsigned gen = 0;
   uint32_t lap = 0;
+  const uint8_t* stp = smem;                         // stage st
+  const uint8_t* const xres = smem + a.xres_off;     // resident activations
+  const uint8_t* xq = xres;                          // ... of this stage's first unit
   for (int f = 0; f < nfill; ++f) {
-    const int k0 = q * U;
-    const int n = a.KT - k0 < U ? a.KT - k0 : U;
+    const bool whole = q < a.QPS - 1 || last_n == U;  // every warp has UPW units in this stage
+    const int n = whole ? U : last_n;
     if (!dead && !warp_wait(full + 8 * st, lap & 1u, a.err)) dead = true;
-    const uint8_t* stp = smem + st * a.stage_bytes;
-    const uint8_t* xp = a.x_res ? smem + a.xres_off + k0 * x_unit : stp + a.x_off;
+    const uint8_t* xp = XRES ? xq : stp + a.x_off;
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j) {
-        const int u = j * kGemvWarps + warp;
-        if (u < n) load_unit(R[j], stp + u * UB, xp + u * x_unit, o);
+        if (whole || j * kGemvWarps + warp < n) {
+          load_w(R[j], stp + woff[j], o);
+          if (!XRES) {
+            load_x(xs[XRES ? 0 : j][0], xp + xoff[j], o, 0);
+            load_x(xs[XRES ? 0 : j][1], xp + xoff[j], o, 1);
+          }
+        }
       }
     }
     // the stage has been read: hand it back; the last warp to do so refills it
@@ -633,17 +648,26 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         if (refill) atomicAdd(ctl, 1);
       }
     }
-    if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+    if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
     if (!dead) {
 #pragma unroll
-      for (int j = 0; j < UPW; ++j)
-        if (j * kGemvWarps + warp < n) mma_unit(R[j], acc);
+      for (int j = 0; j < UPW; ++j) {
+        if (whole || j * kGemvWarps + warp < n) {
+          if (XRES) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              load_x(xs[0][0], xp + xoff[j], o, h);
+              mma_half(R[j], h, xs[0][0], acc[h]);
+            }
+          } else {
+            mma_unit(R[j], xs[XRES ? 0 : j], acc);
+          }
+        }
+      }
     }
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park the partial sums in slot
       // si % R; the eighth warp to do so adds them in warp order.
-      const int slot = si % a.R;
-      const unsigned gen = (unsigned)(si / a.R);
       int bad = 0;
       if (lane == 0) {
         if (red_gen[slot] != gen) {
@@ -694,8 +718,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
       q = 0;
       ++si;
+      if (++slot == a.R) { slot = 0; ++gen; }
+      xq = xres;
+    } else {
+      xq += U * x_unit;
     }
-    if (++st == a.NS) { st = 0; ++lap; }
+    if (++st == a.NS) {
+      st = 0;
+      ++lap;
+      stp = smem;
+    } else {
+      stp += a.stage_bytes;
+    }
   }
   if (dead && lane == 0) atomicOr(ctl + 1, 1);
   __syncthreads();
@@ -829,8 +863,9 @@ int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStre
 
 template <int BITS, int GPT>
 int launch_slab(const SlabArgs& a, int grid, size_t smem, cudaStream_t s) {
-  static std::atomic<unsigned long long> opted{0};
-  return launch_pdl(gemv_slab_kernel<BITS, GPT>, opted, grid, smem, s, a);
+  static std::atomic<unsigned long long> opted_res{0}, opted_stage{0};
+  if (a.x_res) return launch_pdl(gemv_slab_kernel<BITS, GPT, true>, opted_res, grid, smem, s, a);
+  return launch_pdl(gemv_slab_kernel<BITS, GPT, false>, opted_stage, grid, smem, s, a);
 }
 
 // The GEMV of a checked layer with a plan; partials / counters are the
