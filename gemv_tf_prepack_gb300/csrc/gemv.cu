@@ -490,7 +490,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 // to arrive adds the eight in warp order and writes 16 rows of y, so no warp
 // waits for another.
 
-__host__ __device__ constexpr int slab_units_per_warp(int bits) { return bits == 4 ? 2 : 1; }
+// Units per warp per ring stage.  With resident activations a stage holds
+// only weights, so it can be twice as large (fewer handovers per unit).
+__host__ __device__ constexpr int slab_units_per_warp(int bits, bool xres) {
+  return (bits == 4 ? 2 : 1) * (xres ? 2 : 1);
+}
 
 struct SlabArgs {
   const uint8_t* units;
@@ -529,7 +533,7 @@ template <int BITS, int GPT, bool XRES>
 __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uint32_t full, int s0, int f, int st,
                                           bool weights, bool x, int lane) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int U = kGemvWarps * slab_units_per_warp(BITS);
+  constexpr int U = kGemvWarps * slab_units_per_warp(BITS, XRES);
   const int qs = f / a.QPS;
   const int sl = s0 + qs, k0 = (f - qs * a.QPS) * U;
   const int n = a.KT - k0 < U ? a.KT - k0 : U;
@@ -545,12 +549,32 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
   }
 }
 
+// Hand stage st (fill f) back; the last warp to do so refills it with fill
+// f + NS.
+template <int BITS, int GPT, bool XRES>
+__device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbase, uint32_t full, uint32_t empty,
+                                                unsigned* released, int* ctl, int s0, int f, int st, uint32_t lap,
+                                                int nfill, bool dead, int lane) {
+  __syncwarp();
+  unsigned refill = 0;
+  if (lane == 0) {
+    mbar_arrive(empty + 8 * st);
+    if (atomicAdd(released + st, 1u) == kGemvWarps - 1) {
+      released[st] = 0;
+      refill = !dead && f + a.NS < nfill &&
+               mbar_wait(empty + 8 * st, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
+      if (refill) atomicAdd(ctl, 1);
+    }
+  }
+  if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+}
+
 template <int BITS, int GPT, bool XRES>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align128(smem_raw);
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int UPW = slab_units_per_warp(BITS);
+  constexpr int UPW = slab_units_per_warp(BITS, XRES);
   constexpr int U = kGemvWarps * UPW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t = lane & 3;
@@ -609,9 +633,6 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   const int last_n = a.KT - (a.QPS - 1) * U;  // units in the last stage of a slab (1..U)
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   WRegs<BITS, GPT> R[UPW];
-  // Resident activations are read right before their MMAs; per-stage ones
-  // must leave the stage with the weights, before it is handed back.
-  uint32_t xs[XRES ? 1 : UPW][2][8];
   bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
   int st = 0, q = 0, si = 0, slot = 0;
   unsigned gen = 0;
@@ -626,45 +647,27 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     const uint8_t* xp = XRES ? xq : stp + a.x_off;
     if (!dead) {
 #pragma unroll
-      for (int j = 0; j < UPW; ++j) {
-        if (whole || j * kGemvWarps + warp < n) {
-          load_w(R[j], stp + woff[j], o);
-          if (!XRES) {
-            load_x(xs[XRES ? 0 : j][0], xp + xoff[j], o, 0);
-            load_x(xs[XRES ? 0 : j][1], xp + xoff[j], o, 1);
-          }
-        }
-      }
+      for (int j = 0; j < UPW; ++j)
+        if (whole || j * kGemvWarps + warp < n) load_w(R[j], stp + woff[j], o);
     }
-    // the stage has been read: hand it back; the last warp to do so refills it
-    __syncwarp();
-    unsigned refill = 0;
-    if (lane == 0) {
-      mbar_arrive(empty + 8 * st);
-      if (atomicAdd(released + st, 1u) == kGemvWarps - 1) {
-        released[st] = 0;
-        refill = !dead && f + a.NS < nfill &&
-                 mbar_wait(empty + 8 * st, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
-        if (refill) atomicAdd(ctl, 1);
-      }
-    }
-    if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+    // With resident activations the stage is handed back as soon as its
+    // weights are in registers; per-stage activations are read right before
+    // their MMAs, so that stage goes back after them.
+    if (XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, empty, released, ctl, s0, f, st, lap, nfill, dead, lane);
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j) {
         if (whole || j * kGemvWarps + warp < n) {
-          if (XRES) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              load_x(xs[0][0], xp + xoff[j], o, h);
-              mma_half(R[j], h, xs[0][0], acc[h]);
-            }
-          } else {
-            mma_unit(R[j], xs[XRES ? 0 : j], acc);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t xs[8];
+            load_x(xs, xp + xoff[j], o, h);
+            mma_half(R[j], h, xs, acc[h]);
           }
         }
       }
     }
+    if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, empty, released, ctl, s0, f, st, lap, nfill, dead, lane);
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park the partial sums in slot
       // si % R; the eighth warp to do so adds them in warp order.
@@ -792,19 +795,21 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   const int nslab = (Gm.N + kSlabN - 1) / kSlabN;
   if (nslab >= sms && Gm.KT >= kGemvWarps) {
     // Enough slabs for every SM: whole slabs per CTA, at most two CTAs per SM.
-    const int U = kGemvWarps * slab_units_per_warp(Gm.bits);
     const int slots = 2 * sms;
     P->slab = true;
     P->nslab = nslab;
     P->spc = (nslab + slots - 1) / slots;
     P->G = (nslab + P->spc - 1) / P->spc;
-    P->QPS = (Gm.KT + U - 1) / U;
-    const int wbytes = (U * Gm.unit_bytes + 127) / 128 * 128;
-    // x resident in shared memory if that still leaves a ring of 4 stages
+    // x resident in shared memory if that still leaves a ring of two stages
+    const int Ur = kGemvWarps * slab_units_per_warp(Gm.bits, true);
     const int xres = (Gm.KT * M * 256 + 127) / 128 * 128;
-    P->x_off = wbytes;
-    P->x_res = slab_ring(P, wbytes, xres) >= 4;
-    if (P->x_res || slab_ring(P, wbytes + U * M * 256, 0) > 0) return TF_OK;
+    P->QPS = (Gm.KT + Ur - 1) / Ur;
+    P->x_res = slab_ring(P, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres) >= 2;
+    if (P->x_res) return TF_OK;
+    const int Us = kGemvWarps * slab_units_per_warp(Gm.bits, false);
+    P->QPS = (Gm.KT + Us - 1) / Us;
+    P->x_off = (Us * Gm.unit_bytes + 127) / 128 * 128;
+    if (slab_ring(P, P->x_off + Us * M * 256, 0) > 0) return TF_OK;
     *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
   }
   const int TPS = tiles_per_stage(Gm.bits);
