@@ -66,7 +66,7 @@ def source_hash(files):
 
 
 GEMV_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemv.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
-                "gemv_tf_prepack_gb300/csrc/tf_format.h"]
+                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
 GEMM_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemm.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
                 "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
 
