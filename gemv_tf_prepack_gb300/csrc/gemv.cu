@@ -550,21 +550,17 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
 }
 
 // Hand stage st (fill f) back; the last warp to do so refills it with fill
-// f + NS.
+// f + NS.  The release counter's acquire-release atomic orders every warp's
+// reads of the stage before the refill that overwrites it.
 template <int BITS, int GPT, bool XRES>
-__device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbase, uint32_t full, uint32_t empty,
-                                                unsigned* released, int* ctl, int s0, int f, int st, uint32_t lap,
-                                                int nfill, bool dead, int lane) {
+__device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbase, uint32_t full, unsigned* released,
+                                                int* ctl, int s0, int f, int st, int nfill, bool dead, int lane) {
   __syncwarp();
   unsigned refill = 0;
-  if (lane == 0) {
-    mbar_arrive(empty + 8 * st);
-    if (atomicAdd(released + st, 1u) == kGemvWarps - 1) {
-      released[st] = 0;
-      refill = !dead && f + a.NS < nfill &&
-               mbar_wait(empty + 8 * st, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
-      if (refill) atomicAdd(ctl, 1);
-    }
+  if (lane == 0 && atom_add_acq_rel_cta(released + st, 1u) == kGemvWarps - 1) {
+    released[st] = 0;
+    refill = !dead && f + a.NS < nfill;
+    if (refill) atomicAdd(ctl, 1);
   }
   if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
 }
@@ -583,23 +579,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   const int nfill = ns * a.QPS;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full = sbase + (uint32_t)a.ctl_off;
-  const uint32_t empty = full + 8u * a.NS;
-  unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 16 * a.NS);
-  unsigned* red_cnt = released + a.NS;                   // [R] warps that parked a partial
-  volatile unsigned* red_gen = red_cnt + a.R;            // [R] slabs reduced in this slot so far
-  int* ctl = reinterpret_cast<int*>(red_cnt + 2 * a.R);  // [0] fills issued, [1] some wait ran out
+  unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 8 * a.NS);  // [NS] warps done with a stage
+  unsigned* red_cnt = released + a.NS;                                             // [R] warps that parked a partial
+  int* ctl = reinterpret_cast<int*>(red_cnt + a.R);  // [0] fills issued, [1] some wait ran out
   float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [R][8 warps][32 lanes]
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full + 8 * i, XRES ? 1 : 1 + 32);
-      mbar_init(empty + 8 * i, kGemvWarps);
       released[i] = 0;
     }
-    for (int i = 0; i < a.R; ++i) {
-      red_cnt[i] = 0;
-      red_gen[i] = 0;
-    }
+    for (int i = 0; i < a.R; ++i) red_cnt[i] = 0;
     ctl[0] = npre;
     ctl[1] = 0;
     mbar_init_fence();
@@ -635,7 +625,6 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   WRegs<BITS, GPT> R[UPW];
   bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
   int st = 0, q = 0, si = 0, slot = 0;
-  unsigned gen = 0;
   uint32_t lap = 0;
   const uint8_t* stp = smem;                         // stage st
   const uint8_t* const xres = smem + a.xres_off;     // resident activations
@@ -653,7 +642,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     // With resident activations the stage is handed back as soon as its
     // weights are in registers; per-stage activations are read right before
     // their MMAs, so that stage goes back after them.
-    if (XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, empty, released, ctl, s0, f, st, lap, nfill, dead, lane);
+    if (XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j) {
@@ -667,38 +656,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         }
       }
     }
-    if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, empty, released, ctl, s0, f, st, lap, nfill, dead, lane);
+    if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park the partial sums in slot
-      // si % R; the eighth warp to do so adds them in warp order.
-      int bad = 0;
-      if (lane == 0) {
-        if (red_gen[slot] != gen) {
-          // the slot's previous slab is still being reduced (cannot happen
-          // while R exceeds the ring's reach, but never overwrite it)
-          const uint64_t tw = global_timer_ns();
-          while (red_gen[slot] != gen) {
-            if (global_timer_ns() - tw > kGemvTimeoutNs) {
-              atomicCAS(a.err, 0u, kErrGemvWait);
-              bad = 1;
-              break;
-            }
-          }
-        }
-        __threadfence_block();  // acquire: the previous reduction has finished reading the slot
-      }
-      __syncwarp();
-      if (__shfl_sync(0xFFFFFFFFu, bad, 0)) dead = true;
+      // si % R; the eighth warp to do so adds them in warp order.  No warp
+      // can be R slabs ahead of the one reducing a slot (a warp runs at most
+      // NS fills ahead of the slowest, and R > (NS + 1) / QPS), so a slot is
+      // never written while it is being read.
       float4* rb = red + slot * (kGemvWarps * 32);
       rb[warp * 32 + lane] = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
                                          acc[0][3] + acc[1][3]);
       __syncwarp();
       unsigned last = 0;
-      if (lane == 0) {
-        __threadfence_block();  // release this warp's partials
-        last = atomicAdd(red_cnt + slot, 1u) == kGemvWarps - 1;
-        __threadfence_block();  // acquire the other warps' partials
-      }
+      if (lane == 0) last = atom_add_acq_rel_cta(red_cnt + slot, 1u) == kGemvWarps - 1;
       __syncwarp();
       if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -709,11 +679,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         }
         if (!dead) store_y(a.y, a.N, a.M, (s0 + si) * kSlabN + gr, t, v);
         __syncwarp();
-        if (lane == 0) {
-          red_cnt[slot] = 0;
-          __threadfence_block();
-          red_gen[slot] = gen + 1;  // the slot is free for slab si + R
-        }
+        if (lane == 0) red_cnt[slot] = 0;
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -721,7 +687,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
       q = 0;
       ++si;
-      if (++slot == a.R) { slot = 0; ++gen; }
+      if (++slot == a.R) slot = 0;
       xq = xres;
     } else {
       xq += U * x_unit;
@@ -773,7 +739,7 @@ inline int slab_ring(GemvPlan* P, int stage, int xres) {
   for (int ns = 16; ns >= 2; --ns) {
     const int R = clampi((ns - 1 + P->QPS - 1) / P->QPS + 2, 2, 16);
     const int red = R * kGemvWarps * 32 * 16;
-    const int ctl = 16 * ns + 4 * ns + 8 * R + 8;
+    const int ctl = 8 * ns + 4 * ns + 4 * R + 8;
     if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
       P->NS = ns;
       P->R = R;

@@ -124,6 +124,15 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Shared-memory atomic add with acquire-release semantics at CTA scope: this
+// thread's earlier memory accesses (and those ordered before them) happen
+// before it, and its later ones after it.  Returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_cta(const void* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+  return old;
+}
+
 // Wait until every cp.async this thread has issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
