@@ -582,7 +582,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 8 * a.NS);  // [NS] warps done with a stage
   unsigned* red_cnt = released + a.NS;                                             // [R] warps that parked a partial
   int* ctl = reinterpret_cast<int*>(red_cnt + a.R);  // [0] fills issued, [1] some wait ran out
-  float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [R][8 warps][32 lanes]
+  float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [R][8 warps][8 rows][tq lanes]
+  const int tq = (a.M + 1) >> 1;  // lanes per row group holding real tokens
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
@@ -659,25 +660,30 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park the partial sums in slot
-      // si % R; the eighth warp to do so adds them in warp order.  No warp
-      // can be R slabs ahead of the one reducing a slot (a warp runs at most
-      // NS fills ahead of the slowest, and R > (NS + 1) / QPS), so a slot is
-      // never written while it is being read.
-      float4* rb = red + slot * (kGemvWarps * 32);
-      rb[warp * 32 + lane] = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
-                                         acc[0][3] + acc[1][3]);
+      // si % R; the eighth warp to do so adds them in warp order.  A warp
+      // runs at most NS fills ahead of the slowest, and R * QPS >= NS + 1, so
+      // no warp can reach a slot while the warp reducing its previous slab
+      // is still reading it.  Only lanes t < tq hold real tokens (2t, 2t+1).
+      if (t < tq) {
+        float4* rb = red + slot * (kGemvWarps * 8 * tq);
+        rb[warp * 8 * tq + gr * tq + t] = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1],
+                                                      acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
+      }
       __syncwarp();
       unsigned last = 0;
       if (lane == 0) last = atom_add_acq_rel_cta(red_cnt + slot, 1u) == kGemvWarps - 1;
       __syncwarp();
       if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < tq) {
+          const float4* rb = red + slot * (kGemvWarps * 8 * tq) + gr * tq + t;
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) {
-          const float4 u = rb[w * 32 + lane];
-          v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+          for (int w = 0; w < kGemvWarps; ++w) {
+            const float4 u = rb[w * 8 * tq];
+            v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+          }
+          if (!dead) store_y(a.y, a.N, a.M, (s0 + si) * kSlabN + gr, t, v);
         }
-        if (!dead) store_y(a.y, a.N, a.M, (s0 + si) * kSlabN + gr, t, v);
         __syncwarp();
         if (lane == 0) red_cnt[slot] = 0;
       }
@@ -714,7 +720,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
 // ===========================================================================
 // host side
 
-constexpr int kGemvSmemBudget = 110 * 1024;  // ring + control bytes per CTA; two CTAs share an SM
+constexpr int kGemvSmemBudget = 112 * 1024;  // ring + control bytes per CTA; two CTAs share an SM
 constexpr int kGemvSmemMax = 113 * 1024;
 
 struct GemvPlan {
@@ -734,11 +740,12 @@ inline int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v
 
 // Deepest slab-GEMV ring (<= 16 stages) that fits the budget next to the
 // resident x (xres bytes, 0 if none), the reduction slots and the control
-// words; 0 if not even two stages fit.
-inline int slab_ring(GemvPlan* P, int stage, int xres) {
+// words; 0 if not even two stages fit.  R slots with R * QPS >= NS + 1; a
+// slot holds 8 warps x 8 rows x ceil(M/2) lanes of four floats.
+inline int slab_ring(GemvPlan* P, int M, int stage, int xres) {
   for (int ns = 16; ns >= 2; --ns) {
-    const int R = clampi((ns - 1 + P->QPS - 1) / P->QPS + 2, 2, 16);
-    const int red = R * kGemvWarps * 32 * 16;
+    const int R = clampi((ns + P->QPS) / P->QPS, 1, 16);
+    const int red = R * kGemvWarps * 8 * ((M + 1) / 2) * 16;
     const int ctl = 8 * ns + 4 * ns + 4 * R + 8;
     if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
       P->NS = ns;
@@ -770,12 +777,12 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
     const int Ur = kGemvWarps * slab_units_per_warp(Gm.bits, true);
     const int xres = (Gm.KT * M * 256 + 127) / 128 * 128;
     P->QPS = (Gm.KT + Ur - 1) / Ur;
-    P->x_res = slab_ring(P, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres) >= 2;
+    P->x_res = slab_ring(P, M, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres) >= 2;
     if (P->x_res) return TF_OK;
     const int Us = kGemvWarps * slab_units_per_warp(Gm.bits, false);
     P->QPS = (Gm.KT + Us - 1) / Us;
     P->x_off = (Us * Gm.unit_bytes + 127) / 128 * 128;
-    if (slab_ring(P, P->x_off + Us * M * 256, 0) > 0) return TF_OK;
+    if (slab_ring(P, M, P->x_off + Us * M * 256, 0) > 0) return TF_OK;
     *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
   }
   const int TPS = tiles_per_stage(Gm.bits);
