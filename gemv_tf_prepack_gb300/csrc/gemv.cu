@@ -486,9 +486,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 // weight copies already issued to the TMA unit): all of x once, into a
 // resident buffer, when it fits, else each stage's slices with the stage.
 // Warp w takes units w, w + 8, ... of every stage.  At the end of a slab
-// each warp parks its partial sums in a shared-memory slot; the last warp
-// to arrive adds the eight in warp order and writes 16 rows of y, so no warp
-// waits for another.
+// each warp parks its partial sums in its own shared-memory slot and goes
+// on; after the last slab the eight warps add the CTA's slabs in parallel
+// (each slab's eight partials in warp order) and write y, so no warp waits
+// for another inside the stream.
 
 // Units per warp per ring stage.  With resident activations a stage holds
 // only weights, so it can be twice as large (fewer handovers per unit).
@@ -504,7 +505,6 @@ struct SlabArgs {
   int N, K, M, KT, g;
   int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
   int x_res;            // 1: x resident in shared memory; 0: x slices travel with each stage
-  int R;                // reduction slots (a warp is never more than R - 1 slabs ahead of another)
   int NS, stage_bytes, x_off, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
 };
 
@@ -580,17 +580,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full = sbase + (uint32_t)a.ctl_off;
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 8 * a.NS);  // [NS] warps done with a stage
-  unsigned* red_cnt = released + a.NS;                                             // [R] warps that parked a partial
-  int* ctl = reinterpret_cast<int*>(red_cnt + a.R);  // [0] fills issued, [1] some wait ran out
-  float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [R][8 warps][8 rows][tq lanes]
-  const int tq = (a.M + 1) >> 1;  // lanes per row group holding real tokens
+  int* ctl = reinterpret_cast<int*>(released + a.NS);  // [0] fills issued, [1] some wait ran out
+  float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [spc slabs][8 warps][8 rows][tq lanes]
+  const int tq = (a.M + 1) >> 1;  // lanes per row group holding real tokens (2t, 2t + 1)
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full + 8 * i, XRES ? 1 : 1 + 32);
       released[i] = 0;
     }
-    for (int i = 0; i < a.R; ++i) red_cnt[i] = 0;
     ctl[0] = npre;
     ctl[1] = 0;
     mbar_init_fence();
@@ -625,7 +623,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   WRegs<BITS, GPT> R[UPW];
   bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
-  int st = 0, q = 0, si = 0, slot = 0;
+  int st = 0, q = 0, si = 0;
   uint32_t lap = 0;
   const uint8_t* stp = smem;                         // stage st
   const uint8_t* const xres = smem + a.xres_off;     // resident activations
@@ -659,41 +657,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     }
     if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (++q == a.QPS) {
-      // Slab s0 + si is done for this warp: park the partial sums in slot
-      // si % R; the eighth warp to do so adds them in warp order.  A warp
-      // runs at most NS fills ahead of the slowest, and R * QPS >= NS + 1, so
-      // no warp can reach a slot while the warp reducing its previous slab
-      // is still reading it.  Only lanes t < tq hold real tokens (2t, 2t+1).
-      if (t < tq) {
-        float4* rb = red + slot * (kGemvWarps * 8 * tq);
-        rb[warp * 8 * tq + gr * tq + t] = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1],
-                                                      acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
-      }
-      __syncwarp();
-      unsigned last = 0;
-      if (lane == 0) last = atom_add_acq_rel_cta(red_cnt + slot, 1u) == kGemvWarps - 1;
-      __syncwarp();
-      if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-        if (t < tq) {
-          const float4* rb = red + slot * (kGemvWarps * 8 * tq) + gr * tq + t;
-          float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int w = 0; w < kGemvWarps; ++w) {
-            const float4 u = rb[w * 8 * tq];
-            v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
-          }
-          if (!dead) store_y(a.y, a.N, a.M, (s0 + si) * kSlabN + gr, t, v);
-        }
-        __syncwarp();
-        if (lane == 0) red_cnt[slot] = 0;
-      }
+      // Slab s0 + si is done for this warp: park its partial sums (only
+      // lanes t < tq hold real tokens); the slabs are reduced after the loop.
+      if (t < tq)
+        red[((si * kGemvWarps + warp) * 8 + gr) * tq + t] =
+            make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
       q = 0;
       ++si;
-      if (++slot == a.R) slot = 0;
       xq = xres;
     } else {
       xq += U * x_unit;
@@ -708,6 +682,20 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   }
   if (dead && lane == 0) atomicOr(ctl + 1, 1);
   __syncthreads();
+  // Every warp's partial sums of every slab are parked: warp w adds the eight
+  // partials of slabs w, w + 8, ... in warp order and writes their 16 rows.
+  if (!ctl[1] && t < tq) {
+    for (int i = warp; i < ns; i += kGemvWarps) {
+      const float4* rb = red + (i * kGemvWarps * 8 + gr) * tq + t;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) {
+        const float4 u = rb[w * 8 * tq];
+        v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+      }
+      store_y(a.y, a.N, a.M, (s0 + i) * kSlabN + gr, t, v);
+    }
+  }
   if (threadIdx.x == 0 && ctl[1]) {
     // A wait ran out: let the copies still in flight land before the CTA's
     // shared memory goes away.  Only the last NS fills can be outstanding.
@@ -732,24 +720,22 @@ struct GemvPlan {
   int S_max;
   size_t partial_bytes, counter_bytes;
   // slab GEMV
-  int nslab, spc, QPS, x_res, R, xres_off, red_off, ctl_off;
+  int nslab, spc, QPS, x_res, xres_off, red_off, ctl_off;
   size_t smem;
 };
 
 inline int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
 // Deepest slab-GEMV ring (<= 16 stages) that fits the budget next to the
-// resident x (xres bytes, 0 if none), the reduction slots and the control
-// words; 0 if not even two stages fit.  R slots with R * QPS >= NS + 1; a
-// slot holds 8 warps x 8 rows x ceil(M/2) lanes of four floats.
+// resident x (xres bytes, 0 if none), the parked partial sums (spc slabs x
+// 8 warps x 8 rows x ceil(M/2) lanes of four floats) and the control words;
+// 0 if not even two stages fit.
 inline int slab_ring(GemvPlan* P, int M, int stage, int xres) {
+  const int red = P->spc * kGemvWarps * 8 * ((M + 1) / 2) * 16;
   for (int ns = 16; ns >= 2; --ns) {
-    const int R = clampi((ns + P->QPS) / P->QPS, 1, 16);
-    const int red = R * kGemvWarps * 8 * ((M + 1) / 2) * 16;
-    const int ctl = 8 * ns + 4 * ns + 4 * R + 8;
+    const int ctl = 8 * ns + 4 * ns + 8;
     if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
       P->NS = ns;
-      P->R = R;
       P->stage_bytes = stage;
       P->xres_off = ns * stage;
       P->red_off = P->xres_off + xres;
@@ -857,7 +843,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
     SlabArgs a;
     a.units = units; a.x = x; a.y = y; a.err = err;
     a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
-    a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS; a.x_res = P.x_res; a.R = P.R;
+    a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS; a.x_res = P.x_res;
     a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off; a.xres_off = P.xres_off;
     a.red_off = P.red_off; a.ctl_off = P.ctl_off;
     if (G.bits == 4) {

@@ -53,8 +53,9 @@ __device__ __forceinline__ MetaW4 meta_w4(uint32_t scale_pair, uint32_t zero_byt
   MetaW4 m;
   m.s_lo = __byte_perm(scale_pair, 0, 0x1010);
   m.s_hi = __byte_perm(scale_pair, 0, 0x3232);
-  m.z_lo = ((zero_byte & 0xFu) * 0x00010001u) | 0x43004300u;
-  m.z_hi = (((zero_byte >> 4) & 0xFu) * 0x00010001u) | 0x43004300u;
+  const uint32_t zz = __byte_perm(zero_byte, 0, 0x4040);  // the zero byte in bytes 0 and 2
+  m.z_lo = and_or(zz, 0x000F000Fu, 0x43004300u);
+  m.z_hi = and_or(zz >> 4, 0x000F000Fu, 0x43004300u);
   return m;
 }
 
