@@ -582,6 +582,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.ctl_off + 8 * a.NS);  // [NS] warps done with a stage
   int* ctl = reinterpret_cast<int*>(released + a.NS);  // [0] fills issued, [1] some wait ran out
   float4* red = reinterpret_cast<float4*>(smem + a.red_off);  // [spc slabs][8 warps][8 rows][tq lanes]
+  float2* red2 = reinterpret_cast<float2*>(red);               // M = 1: [spc slabs][8 warps][8 rows]
   const int tq = (a.M + 1) >> 1;  // lanes per row group holding real tokens (2t, 2t + 1)
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
@@ -659,9 +660,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park its partial sums (only
       // lanes t < tq hold real tokens); the slabs are reduced after the loop.
-      if (t < tq)
+      if (a.M == 1) {  // one token: only (row gr, token 0) and (row gr + 8, token 0) are real
+        if (t == 0)
+          red2[(si * kGemvWarps + warp) * 8 + gr] = make_float2(acc[0][0] + acc[1][0], acc[0][2] + acc[1][2]);
+      } else if (t < tq) {
         red[((si * kGemvWarps + warp) * 8 + gr) * tq + t] =
             make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -686,12 +691,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   // partials of slabs w, w + 8, ... in warp order and writes their 16 rows.
   if (!ctl[1] && t < tq) {
     for (int i = warp; i < ns; i += kGemvWarps) {
-      const float4* rb = red + (i * kGemvWarps * 8 + gr) * tq + t;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (a.M == 1) {
+        const float2* rb = red2 + i * kGemvWarps * 8 + gr;
 #pragma unroll
-      for (int w = 0; w < kGemvWarps; ++w) {
-        const float4 u = rb[w * 8 * tq];
-        v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+        for (int w = 0; w < kGemvWarps; ++w) {
+          const float2 u = rb[w * 8];
+          v[0] += u.x; v[2] += u.y;
+        }
+      } else {
+        const float4* rb = red + (i * kGemvWarps * 8 + gr) * tq + t;
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) {
+          const float4 u = rb[w * 8 * tq];
+          v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
+        }
       }
       store_y(a.y, a.N, a.M, (s0 + i) * kSlabN + gr, t, v);
     }
@@ -708,8 +722,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
 // ===========================================================================
 // host side
 
-constexpr int kGemvSmemBudget = 112 * 1024;  // ring + control bytes per CTA; two CTAs share an SM
+// Two CTAs per SM: 2 x (113 KB + 1 KB the runtime reserves per CTA) = 228 KB.
 constexpr int kGemvSmemMax = 113 * 1024;
+constexpr int kGemvSmemBudget = kGemvSmemMax - 128;  // ring + control bytes (128 for the alignment slack)
 
 struct GemvPlan {
   bool slab;  // slab GEMV (else tile GEMV)
@@ -730,9 +745,9 @@ inline int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v
 // resident x (xres bytes, 0 if none), the parked partial sums (spc slabs x
 // 8 warps x 8 rows x ceil(M/2) lanes of four floats) and the control words;
 // 0 if not even two stages fit.
-inline int slab_ring(GemvPlan* P, int M, int stage, int xres) {
-  const int red = P->spc * kGemvWarps * 8 * ((M + 1) / 2) * 16;
-  for (int ns = 16; ns >= 2; --ns) {
+inline int slab_ring(GemvPlan* P, int M, int stage, int xres, int max_ns) {
+  const int red = P->spc * kGemvWarps * 8 * (M == 1 ? 8 : ((M + 1) / 2) * 16);
+  for (int ns = max_ns; ns >= 2; --ns) {
     const int ctl = 8 * ns + 4 * ns + 8;
     if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
       P->NS = ns;
@@ -763,12 +778,15 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
     const int Ur = kGemvWarps * slab_units_per_warp(Gm.bits, true);
     const int xres = (Gm.KT * M * 256 + 127) / 128 * 128;
     P->QPS = (Gm.KT + Ur - 1) / Ur;
-    P->x_res = slab_ring(P, M, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres) >= 2;
+    // Two stages of 32 units: a deeper prefetch makes the flood at the start
+    // of each layer larger, and the activation load that every warp waits
+    // for queues behind it (the decode step measured 1 us slower with three).
+    P->x_res = slab_ring(P, M, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres, 2) >= 2;
     if (P->x_res) return TF_OK;
     const int Us = kGemvWarps * slab_units_per_warp(Gm.bits, false);
     P->QPS = (Gm.KT + Us - 1) / Us;
     P->x_off = (Us * Gm.unit_bytes + 127) / 128 * 128;
-    if (slab_ring(P, M, P->x_off + Us * M * 256, 0) > 0) return TF_OK;
+    if (slab_ring(P, M, P->x_off + Us * M * 256, 0, 16) > 0) return TF_OK;
     *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
   }
   const int TPS = tiles_per_stage(Gm.bits);
