@@ -485,16 +485,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 // copied with 16-byte cp.async (load/store path, so they do not queue behind
 // weight copies already issued to the TMA unit): all of x once, into a
 // resident buffer, when it fits, else each stage's slices with the stage.
-// Warp w takes units w, w + 8, ... of every stage.  At the end of a slab
+// A CTA has eight warps (two CTAs per SM) or, when x is too large to stay
+// resident next to a useful ring at two CTAs per SM, sixteen (one per SM).
+// Warp w takes units w, w + NW, ... of every stage.  At the end of a slab
 // each warp parks its partial sums in its own shared-memory slot and goes
 // on; after the last slab the eight warps add the CTA's slabs in parallel
 // (each slab's eight partials in warp order) and write y, so no warp waits
 // for another inside the stream.
 
-// Units per warp per ring stage.  With resident activations a stage holds
-// only weights, so it can be twice as large (fewer handovers per unit).
-__host__ __device__ constexpr int slab_units_per_warp(int bits, bool xres) {
-  return (bits == 4 ? 2 : 1) * (xres ? 2 : 1);
+// Units per warp per ring stage.  With resident activations a stage of the
+// eight-warp configuration holds only weights, so it can be twice as large
+// (fewer handovers per unit).
+__host__ __device__ constexpr int slab_units_per_warp(int bits, bool xres, int nw) {
+  return (bits == 4 ? 2 : 1) * (xres && nw == 8 ? 2 : 1);
 }
 
 struct SlabArgs {
@@ -529,11 +532,11 @@ __device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int k0, 
 // by lane 0.  Per-stage activations (x_res == 0): all 32 lanes copy 16-byte
 // chunks and each lane then arrives on the stage's barrier once its copies
 // have landed (the barrier then expects 1 + 32 arrivals per fill).
-template <int BITS, int GPT, bool XRES>
+template <int BITS, int GPT, bool XRES, int NW>
 __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uint32_t full, int s0, int f, int st,
                                           bool weights, bool x, int lane) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int U = kGemvWarps * slab_units_per_warp(BITS, XRES);
+  constexpr int U = NW * slab_units_per_warp(BITS, XRES, NW);
   const int qs = f / a.QPS;
   const int sl = s0 + qs, k0 = (f - qs * a.QPS) * U;
   const int n = a.KT - k0 < U ? a.KT - k0 : U;
@@ -552,26 +555,26 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
 // Hand stage st (fill f) back; the last warp to do so refills it with fill
 // f + NS.  The release counter's acquire-release atomic orders every warp's
 // reads of the stage before the refill that overwrites it.
-template <int BITS, int GPT, bool XRES>
+template <int BITS, int GPT, bool XRES, int NW>
 __device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbase, uint32_t full, unsigned* released,
                                                 int* ctl, int s0, int f, int st, int nfill, bool dead, int lane) {
   __syncwarp();
   unsigned refill = 0;
-  if (lane == 0 && atom_add_acq_rel_cta(released + st, 1u) == kGemvWarps - 1) {
+  if (lane == 0 && atom_add_acq_rel_cta(released + st, 1u) == NW - 1) {
     released[st] = 0;
     refill = !dead && f + a.NS < nfill;
     if (refill) atomicAdd(ctl, 1);
   }
-  if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+  if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
 }
 
-template <int BITS, int GPT, bool XRES>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabArgs a) {
+template <int BITS, int GPT, bool XRES, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(const SlabArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align128(smem_raw);
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int UPW = slab_units_per_warp(BITS, XRES);
-  constexpr int U = kGemvWarps * UPW;
+  constexpr int UPW = slab_units_per_warp(BITS, XRES, NW);
+  constexpr int U = NW * UPW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t = lane & 3;
   const int s0 = blockIdx.x * a.spc;
@@ -598,16 +601,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   if (warp == 0) {
     if (lane == 0) griddep_launch_dependents();
     // static weights first, before the grid dependency resolves
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f, f, true, false, lane);
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
   }
   // y and x may still be in use by the previous grid
   griddep_wait();
   if (XRES) {
-    copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, kGemvThreads);
+    copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, NW * 32);
     cp_async_wait_all();
     __syncthreads();
   } else if (warp == 0) {
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES>(a, sbase, full, s0, f, f, false, true, lane);
+    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, false, true, lane);
   }
 
   const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
@@ -617,8 +620,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   int woff[UPW], xoff[UPW];
 #pragma unroll
   for (int j = 0; j < UPW; ++j) {
-    woff[j] = (j * kGemvWarps + warp) * UB;
-    xoff[j] = (j * kGemvWarps + warp) * x_unit;
+    woff[j] = (j * NW + warp) * UB;
+    xoff[j] = (j * NW + warp) * x_unit;
   }
   const int last_n = a.KT - (a.QPS - 1) * U;  // units in the last stage of a slab (1..U)
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -637,16 +640,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j)
-        if (whole || j * kGemvWarps + warp < n) load_w(R[j], stp + woff[j], o);
+        if (whole || j * NW + warp < n) load_w(R[j], stp + woff[j], o);
     }
     // With resident activations the stage is handed back as soon as its
     // weights are in registers; per-stage activations are read right before
     // their MMAs, so that stage goes back after them.
-    if (XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
+    if (XRES) hand_back_stage<BITS, GPT, XRES, NW>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j) {
-        if (whole || j * kGemvWarps + warp < n) {
+        if (whole || j * NW + warp < n) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t xs[8];
@@ -656,15 +659,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
         }
       }
     }
-    if (!XRES) hand_back_stage<BITS, GPT, XRES>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
+    if (!XRES) hand_back_stage<BITS, GPT, XRES, NW>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park its partial sums (only
       // lanes t < tq hold real tokens); the slabs are reduced after the loop.
       if (a.M == 1) {  // one token: only (row gr, token 0) and (row gr + 8, token 0) are real
         if (t == 0)
-          red2[(si * kGemvWarps + warp) * 8 + gr] = make_float2(acc[0][0] + acc[1][0], acc[0][2] + acc[1][2]);
+          red2[(si * NW + warp) * 8 + gr] = make_float2(acc[0][0] + acc[1][0], acc[0][2] + acc[1][2]);
       } else if (t < tq) {
-        red[((si * kGemvWarps + warp) * 8 + gr) * tq + t] =
+        red[((si * NW + warp) * 8 + gr) * tq + t] =
             make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
       }
 #pragma unroll
@@ -690,19 +693,19 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
   // Every warp's partial sums of every slab are parked: warp w adds the eight
   // partials of slabs w, w + 8, ... in warp order and writes their 16 rows.
   if (!ctl[1] && t < tq) {
-    for (int i = warp; i < ns; i += kGemvWarps) {
+    for (int i = warp; i < ns; i += NW) {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (a.M == 1) {
-        const float2* rb = red2 + i * kGemvWarps * 8 + gr;
+        const float2* rb = red2 + i * NW * 8 + gr;
 #pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
           const float2 u = rb[w * 8];
           v[0] += u.x; v[2] += u.y;
         }
       } else {
-        const float4* rb = red + (i * kGemvWarps * 8 + gr) * tq + t;
+        const float4* rb = red + (i * NW * 8 + gr) * tq + t;
 #pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
           const float4 u = rb[w * 8 * tq];
           v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
         }
@@ -723,7 +726,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_slab_kernel(const SlabAr
 // host side
 
 // Two CTAs per SM: 2 x (113 KB + 1 KB the runtime reserves per CTA) = 228 KB.
+// One CTA per SM (the 16-warp slab configuration): 227 KB.
 constexpr int kGemvSmemMax = 113 * 1024;
+constexpr int kGemvSmemMax1 = 227 * 1024;
 constexpr int kGemvSmemBudget = kGemvSmemMax - 128;  // ring + control bytes (128 for the alignment slack)
 
 struct GemvPlan {
@@ -735,21 +740,22 @@ struct GemvPlan {
   int S_max;
   size_t partial_bytes, counter_bytes;
   // slab GEMV
+  int nw;  // warps per CTA: 8 (two CTAs per SM) or 16 (one CTA per SM)
   int nslab, spc, QPS, x_res, xres_off, red_off, ctl_off;
   size_t smem;
 };
 
 inline int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
-// Deepest slab-GEMV ring (<= 16 stages) that fits the budget next to the
-// resident x (xres bytes, 0 if none), the parked partial sums (spc slabs x
-// 8 warps x 8 rows x ceil(M/2) lanes of four floats) and the control words;
-// 0 if not even two stages fit.
-inline int slab_ring(GemvPlan* P, int M, int stage, int xres, int max_ns) {
-  const int red = P->spc * kGemvWarps * 8 * (M == 1 ? 8 : ((M + 1) / 2) * 16);
+// Deepest slab-GEMV ring (<= max_ns stages) that fits the budget next to
+// the resident x (xres bytes, 0 if none), the parked partial sums (spc slabs
+// x nw warps x 8 rows x ceil(M/2) lanes of four floats; two floats at M = 1)
+// and the control words; 0 if not even two stages fit.
+inline int slab_ring(GemvPlan* P, int M, int stage, int xres, int max_ns, int budget) {
+  const int red = P->spc * P->nw * 8 * (M == 1 ? 8 : ((M + 1) / 2) * 16);
   for (int ns = max_ns; ns >= 2; --ns) {
     const int ctl = 8 * ns + 4 * ns + 8;
-    if (ns * stage + xres + red + ctl <= kGemvSmemBudget) {
+    if (ns * stage + xres + red + ctl <= budget) {
       P->NS = ns;
       P->stage_bytes = stage;
       P->xres_off = ns * stage;
@@ -768,25 +774,38 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   *P = GemvPlan{};
   const int nslab = (Gm.N + kSlabN - 1) / kSlabN;
   if (nslab >= sms && Gm.KT >= kGemvWarps) {
-    // Enough slabs for every SM: whole slabs per CTA, at most two CTAs per SM.
-    const int slots = 2 * sms;
+    // Enough slabs for every SM: whole slabs per CTA.
     P->slab = true;
     P->nslab = nslab;
-    P->spc = (nslab + slots - 1) / slots;
-    P->G = (nslab + P->spc - 1) / P->spc;
-    // x resident in shared memory if that still leaves a ring of two stages
-    const int Ur = kGemvWarps * slab_units_per_warp(Gm.bits, true);
     const int xres = (Gm.KT * M * 256 + 127) / 128 * 128;
-    P->QPS = (Gm.KT + Ur - 1) / Ur;
-    // Two stages of 32 units: a deeper prefetch makes the flood at the start
-    // of each layer larger, and the activation load that every warp waits
-    // for queues behind it (the decode step measured 1 us slower with three).
-    P->x_res = slab_ring(P, M, (Ur * Gm.unit_bytes + 127) / 128 * 128, xres, 2) >= 2;
+    // (1) Eight warps, two CTAs per SM, x resident next to a ring of two
+    // 32-unit stages: a deeper prefetch makes the flood at the start of each
+    // layer larger, and the activation load every warp waits for queues
+    // behind it (three stages cost the four-layer decode step about 1 us).
+    P->nw = 8;
+    P->spc = (nslab + 2 * sms - 1) / (2 * sms);
+    P->G = (nslab + P->spc - 1) / P->spc;
+    const int U8 = 8 * slab_units_per_warp(Gm.bits, true, 8);
+    P->QPS = (Gm.KT + U8 - 1) / U8;
+    P->x_res = slab_ring(P, M, (U8 * Gm.unit_bytes + 127) / 128 * 128, xres, 2, kGemvSmemBudget) >= 2;
     if (P->x_res) return TF_OK;
-    const int Us = kGemvWarps * slab_units_per_warp(Gm.bits, false);
+    // (2) x too large for that: sixteen warps, one CTA per SM, x resident
+    // next to a ring of up to four stages.
+    P->nw = 16;
+    P->spc = (nslab + sms - 1) / sms;
+    P->G = (nslab + P->spc - 1) / P->spc;
+    const int U16 = 16 * slab_units_per_warp(Gm.bits, true, 16);
+    P->QPS = (Gm.KT + U16 - 1) / U16;
+    P->x_res = slab_ring(P, M, (U16 * Gm.unit_bytes + 127) / 128 * 128, xres, 4, kGemvSmemMax1 - 128) >= 3;
+    if (P->x_res) return TF_OK;
+    // (3) Eight warps, two CTAs per SM, x slices travelling with each stage.
+    P->nw = 8;
+    P->spc = (nslab + 2 * sms - 1) / (2 * sms);
+    P->G = (nslab + P->spc - 1) / P->spc;
+    const int Us = 8 * slab_units_per_warp(Gm.bits, false, 8);
     P->QPS = (Gm.KT + Us - 1) / Us;
     P->x_off = (Us * Gm.unit_bytes + 127) / 128 * 128;
-    if (slab_ring(P, M, P->x_off + Us * M * 256, 0, 16) > 0) return TF_OK;
+    if (slab_ring(P, M, P->x_off + Us * M * 256, 0, 16, kGemvSmemBudget) > 0) return TF_OK;
     *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
   }
   const int TPS = tiles_per_stage(Gm.bits);
@@ -809,20 +828,20 @@ inline size_t gemv_scratch_bytes(const GemvPlan& P) { return P.slab ? 0 : P.part
 // Launch with programmatic dependent launch; opts the kernel in, once per
 // device, to the largest ring a plan can ask for.
 template <class Kern, class... Args>
-int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, size_t smem, cudaStream_t s,
-               Args... args) {
+int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, int threads, int smem_max, size_t smem,
+               cudaStream_t s, Args... args) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
   if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax) != cudaSuccess ||
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
         cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return TF_ERR_CUDA;
     opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }
-  if (smem > (size_t)kGemvSmemMax) return TF_ERR_UNSUPPORTED;
+  if (smem > (size_t)smem_max) return TF_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemvThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -840,14 +859,16 @@ int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, size_
 template <int BITS, int GPT>
 int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
   static std::atomic<unsigned long long> opted{0};
-  return launch_pdl(gemv_kernel<BITS, GPT>, opted, a.G, smem, s, map, a);
+  return launch_pdl(gemv_kernel<BITS, GPT>, opted, a.G, kGemvThreads, kGemvSmemMax, smem, s, map, a);
 }
 
 template <int BITS, int GPT>
-int launch_slab(const SlabArgs& a, int grid, size_t smem, cudaStream_t s) {
-  static std::atomic<unsigned long long> opted_res{0}, opted_stage{0};
-  if (a.x_res) return launch_pdl(gemv_slab_kernel<BITS, GPT, true>, opted_res, grid, smem, s, a);
-  return launch_pdl(gemv_slab_kernel<BITS, GPT, false>, opted_stage, grid, smem, s, a);
+int launch_slab(const SlabArgs& a, int nw, int grid, size_t smem, cudaStream_t s) {
+  static std::atomic<unsigned long long> opted_res{0}, opted_res16{0}, opted_stage{0};
+  if (a.x_res && nw == 16)
+    return launch_pdl(gemv_slab_kernel<BITS, GPT, true, 16>, opted_res16, grid, 512, kGemvSmemMax1, smem, s, a);
+  if (a.x_res) return launch_pdl(gemv_slab_kernel<BITS, GPT, true, 8>, opted_res, grid, 256, kGemvSmemMax, smem, s, a);
+  return launch_pdl(gemv_slab_kernel<BITS, GPT, false, 8>, opted_stage, grid, 256, kGemvSmemMax, smem, s, a);
 }
 
 // The GEMV of a checked layer with a plan; partials / counters are the
@@ -865,13 +886,13 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
     a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off; a.xres_off = P.xres_off;
     a.red_off = P.red_off; a.ctl_off = P.ctl_off;
     if (G.bits == 4) {
-      if (G.gpt == 1) return launch_slab<4, 1>(a, P.G, P.smem, stream);
-      if (G.gpt == 2) return launch_slab<4, 2>(a, P.G, P.smem, stream);
-      return launch_slab<4, 4>(a, P.G, P.smem, stream);
+      if (G.gpt == 1) return launch_slab<4, 1>(a, P.nw, P.G, P.smem, stream);
+      if (G.gpt == 2) return launch_slab<4, 2>(a, P.nw, P.G, P.smem, stream);
+      return launch_slab<4, 4>(a, P.nw, P.G, P.smem, stream);
     }
-    if (G.gpt == 1) return launch_slab<8, 1>(a, P.G, P.smem, stream);
-    if (G.gpt == 2) return launch_slab<8, 2>(a, P.G, P.smem, stream);
-    return launch_slab<8, 4>(a, P.G, P.smem, stream);
+    if (G.gpt == 1) return launch_slab<8, 1>(a, P.nw, P.G, P.smem, stream);
+    if (G.gpt == 2) return launch_slab<8, 2>(a, P.nw, P.G, P.smem, stream);
+    return launch_slab<8, 4>(a, P.nw, P.G, P.smem, stream);
   }
   CUtensorMap map;
   int rc = encode_x_map(x, M, G.K, &map);
