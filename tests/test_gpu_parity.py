@@ -148,3 +148,23 @@ def test_gemm_even_blocks(N, K, bits, group, M):
     y = to_host_bits(tf.gemm(W, to_dev_bf16(xb)))
     ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
     check_close(y, ref, f"gemm {N}x{K} w{bits} g{group} M={M}")
+
+
+# Long K: x no longer fits next to a ring at two CTAs per SM, so the slab GEMV
+# runs sixteen warps per CTA with x resident (the first three), or carries x
+# with every stage (M = 8).  Sampled output rows: the oracle row by row.
+LONG_K = [
+    (2440, 24576, 4, 32, 1), (2432, 16384, 8, 64, 2), (2432, 32768, 4, 128, 1), (2440, 16384, 4, 128, 8),
+]
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", LONG_K)
+def test_gemv_slab_long_k(N, K, bits, group, M):
+    assert tf.gemv_workspace_size(N, K, bits, group, M) == 0  # slab GEMV
+    qw, W = layer(N, K, bits, group, 27)
+    xb = synth.make_activations(M, K, 27)
+    y = to_host_bits(tf.gemv(W, to_dev_bf16(xb)))
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(N - 40, N),
+                                     np.random.default_rng(0).integers(0, N, 64)]))
+    ref = tf_oracle.reference_rows(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb, rows)
+    check_close(y[:, rows], ref, f"long-K slab gemv {N}x{K} w{bits} g{group} M={M}")
