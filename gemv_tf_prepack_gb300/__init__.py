@@ -22,7 +22,8 @@ import numpy as np
 
 __all__ = [
     "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "unprepack",
-    "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemv_noalloc", "gemm", "device_error",
+    "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemv_noalloc", "gemm",
+    "gemm_workspace_size", "device_error",
     "header_declarations",
 ]
 
@@ -57,7 +58,8 @@ _SIGNATURES = {
     "tf_dequant": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p]),
     "tf_gemv_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tf_gemv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
-    "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
+    "tf_gemm_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
     "tf_gemv_noalloc": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
     "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -184,12 +186,13 @@ class Weights:
     def nbytes(self) -> int:
         return self.blob.numel()
 
-    def workspace(self, M: int):
-        """A zero-filled GEMV workspace for this layer and M (cached)."""
+    def workspace(self, M: int, kind: str = "gemv"):
+        """A zero-filled GEMV or GEMM workspace for this layer and M (cached)."""
         torch = _torch()
-        key = (M, self.blob.device)
+        key = (kind, M, self.blob.device)
         if key not in self._ws:
-            n = gemv_workspace_size(self.N, self.K, self.bits, self.group, M)
+            size = gemv_workspace_size if kind == "gemv" else gemm_workspace_size
+            n = size(self.N, self.K, self.bits, self.group, M)
             self._ws[key] = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.blob.device)
         return self._ws[key]
 
@@ -253,13 +256,29 @@ def gemv_noalloc(W: Weights, x, y=None, stream=None):
     return y
 
 
-def gemm(W: Weights, x, y=None, stream=None):
-    """y[M, N] = x[M, K] W^T for any M (fused dequant to SMEM + tcgen05 MMAs)."""
+def gemm_workspace_size(N: int, K: int, bits: int, group: int, M: int) -> int:
+    out = _sz()
+    _check(_lib().tf_gemm_workspace_size(N, K, bits, group, M, ctypes.byref(out)), "tf_gemm_workspace_size")
+    return out.value
+
+
+def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True):
+    """y[M, N] = x[M, K] W^T for any M (fused dequant to SMEM + tcgen05 MMAs).
+
+    With stream_k (default) the layer's cached workspace lets the last,
+    partial wave of output tiles be split along K across all SMs; with
+    stream_k False every tile is computed whole by one SM.
+    """
     _check_x(W, x)
     M = x.shape[0]
     y = _out(W, M, y)
+    if stream_k:
+        ws = W.workspace(M, "gemm") if workspace is None else workspace
+        wp, wn = _ptr(ws), ws.numel() * ws.element_size()
+    else:
+        wp, wn = None, 0
     _check(_lib().tf_gemm(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
-                          _stream(stream)), "tf_gemm")
+                          wp, wn, _stream(stream)), "tf_gemm")
     return y
 
 

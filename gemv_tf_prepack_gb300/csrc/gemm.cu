@@ -39,6 +39,7 @@ namespace {
 constexpr int kThreads = 704;        // 22 warps
 constexpr int kDequantWarp0 = 6;     // warps 6..21: (row block, slab) pairs
 constexpr int kEpilogueWarp0 = 2;    // warps 2..5
+constexpr int kEpilogueThreads = 128;
 constexpr int kSlabBytesW = 128 * 128;  // 128 rows x 64 BF16
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr uint64_t kTimeoutNs = 4000000000ull;
@@ -55,15 +56,84 @@ struct GemmArgs {
   const uint8_t* units;
   uint16_t* y;
   unsigned* err;              // device error word
+  float* ws;                  // stream-K partial sums: [CTA][2][BN / 16][128 rows][16]
+  unsigned* cnt;              // stream-K arrivals per tile (zero on entry and on exit)
   int N, K, M, KT, g, tile_bytes;  // tile_bytes: one packed tile (eight units) in shared memory
   int MT, BN, ntiles;
+  int dp_tiles;               // tiles [0, dp_tiles) whole per CTA; the rest split along K
+  int sk_ctas;                // CTAs [0, sk_ctas) share the split tiles' k-iterations (at least one each)
   int P, OPS;                 // stages of the packed ring and of the operand ring
   int off_op, off_bar;        // byte offsets in the 1024-aligned dynamic smem
 };
 
 struct Bars {
-  uint32_t full_p, empty_p, full_op, empty_op, tfull, tempty, drain, tmem_slot;
+  uint32_t full_p, empty_p, full_op, empty_op, tfull, tempty, drain, tmem_slot, flag;
 };
+
+// ---------------------------------------------------------------------------
+// Schedule.  The output tiles (128 weight rows x BN tokens, token index
+// fastest) that do not fill a whole wave of CTAs (all tiles, when there are
+// fewer tiles than CTAs and splitting pays) are split along K ("stream-K"):
+// the k-iterations of tiles [dp_tiles, ntiles) are divided evenly over CTAs
+// [0, sk_ctas) in order (a few CTAs per split tile, at most all of them, and
+// at most the number of those k-iterations, so that no range is empty).  The
+// other tiles are processed whole, CTA c taking tiles c, c + G, ...  Every
+// role of a CTA walks the same sequence: its stream-K segments first, then
+// its whole tiles.
+
+struct Work {
+  int tile, kb, ke;  // k-tiles [kb, ke) of output tile `tile`
+};
+
+struct Sched {
+  long long pos, end;  // this CTA's stream-K k-iterations still to hand out
+  int dp_next;
+};
+
+__device__ __forceinline__ long long sk_begin(const GemmArgs& a, long long c) {
+  return (long long)(a.ntiles - a.dp_tiles) * a.KT * (c < a.sk_ctas ? c : a.sk_ctas) / a.sk_ctas;
+}
+
+__device__ __forceinline__ Sched sched_begin(const GemmArgs& a) {
+  Sched s;
+  s.pos = sk_begin(a, blockIdx.x);
+  s.end = sk_begin(a, blockIdx.x + 1);
+  s.dp_next = blockIdx.x;
+  return s;
+}
+
+__device__ __forceinline__ bool sched_next(const GemmArgs& a, Sched& s, Work& w) {
+  if (s.pos < s.end) {
+    const int ti = (int)(s.pos / a.KT);
+    const long long t_end = (long long)(ti + 1) * a.KT;
+    w.tile = a.dp_tiles + ti;
+    w.kb = (int)(s.pos - (long long)ti * a.KT);
+    w.ke = (int)((s.end < t_end ? s.end : t_end) - (long long)ti * a.KT);
+    s.pos = (long long)ti * a.KT + w.ke;
+    return true;
+  }
+  if (s.dp_next < a.dp_tiles) {
+    w.tile = s.dp_next;
+    w.kb = 0;
+    w.ke = a.KT;
+    s.dp_next += gridDim.x;
+    return true;
+  }
+  return false;
+}
+
+// CTA whose stream-K range holds k-iteration x.
+__device__ __forceinline__ int sk_cta_of(const GemmArgs& a, long long x) {
+  const long long total = (long long)(a.ntiles - a.dp_tiles) * a.KT;
+  return (int)(((x + 1) * a.sk_ctas - 1) / total);
+}
+
+// Partial-sum slot of CTA c's segment of stream-K tile ti: 0 for the tile its
+// range starts in, 1 for the tile its range ends in.
+__device__ __forceinline__ float* sk_slot(const GemmArgs& a, int c, int ti) {
+  const int first = (int)(sk_begin(a, c) / a.KT);
+  return a.ws + ((size_t)c * 2 + (ti == first ? 0 : 1)) * ((size_t)128 * a.BN);
+}
 
 __device__ __forceinline__ Bars bars_at(uint32_t base, int P, int OPS) {
   Bars b;
@@ -75,6 +145,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int P, int OPS) {
   b.tempty = b.tfull + 16;
   b.drain = b.tempty + 16;
   b.tmem_slot = b.drain + 8;
+  b.flag = b.tmem_slot + 8;
   return b;
 }
 
@@ -124,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int ps = 0, os = 0;
       uint32_t pph = 0, oph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-        const int nb = tile / a.MT, mt = tile - nb * a.MT;
-        for (int kt = 0; kt < a.KT && ok; ++kt) {
+      Sched sc = sched_begin(a);
+      Work wk;
+      while (ok && sched_next(a, sc, wk)) {
+        const int nb = wk.tile / a.MT, mt = wk.tile - nb * a.MT;
+        for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
           ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
           if (!ok) break;
           mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
@@ -155,12 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t oph = 0, aph = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
+      Sched sc = sched_begin(a);
+      Work wk;
+      while (ok && sched_next(a, sc, wk)) {
         ok = mbar_wait(B.tempty + 8 * acc, aph ^ 1, err, kErrMmaWait, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * 256;
-        const int nslabs = 2 * a.KT;
+        const int nslabs = 2 * (wk.ke - wk.kb);
         for (int sl = 0; sl < nslabs; ++sl) {
           ok = mbar_wait(B.full_op + 8 * os, oph, err, kErrMmaWait, kTimeoutNs);
           if (!ok) break;
@@ -187,35 +262,109 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else if (warp >= kEpilogueWarp0 && warp < kDequantWarp0) {
     // ---------------------------------------------------------------- epilogue
+    // Thread (q, lane) owns accumulator row q*32 + lane.  A whole tile goes
+    // straight to y.  A stream-K segment is stored as FP32 partial sums
+    // ([BN/16][128 rows][16]: 64 contiguous bytes per thread per step); the
+    // last of the tile's contributors adds all of them in CTA order (a fixed
+    // order: the same result every run) and writes y.
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    volatile unsigned* flag = reinterpret_cast<volatile unsigned*>(smem + (B.flag - sbase));
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-      const int nb = tile / a.MT, mt = tile - nb * a.MT;
+    Sched sc = sched_begin(a);
+    Work wk;
+    while (ok && sched_next(a, sc, wk)) {
+      const int nb = wk.tile / a.MT, mt = wk.tile - nb * a.MT;
       ok = mbar_wait(B.tfull + 8 * acc, aph, err, kErrEpilogueWait, kTimeoutNs);
+      // the four epilogue warps meet at named barriers below: they must all
+      // go on, or all stop
+      ok = named_barrier_and(kEpilogueThreads, ok);
       if (!ok) break;
       tc_fence_after();
-      const int n = nb * kTileN + q * 32 + lane;
+      const int n = nb * kTileN + row;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256;
+      const bool whole = wk.kb == 0 && wk.ke == a.KT;
+      const int ti = wk.tile - a.dp_tiles;
+      float* mine = whole ? nullptr : sk_slot(a, blockIdx.x, ti);
       for (int c0 = 0; c0 < a.BN; c0 += 16) {
         uint32_t r[16];
         tmem_ld_16(taddr + (uint32_t)c0, r);
         tmem_ld_wait();
-        const int m0 = mt * a.BN + c0;
-        if (n < a.N) {
+        if (whole) {
+          const int m0 = mt * a.BN + c0;
+          if (n < a.N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = m0 + j;
-            if (m < a.M)
-              a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+            for (int j = 0; j < 16; ++j) {
+              const int m = m0 + j;
+              if (m < a.M)
+                a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+            }
           }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(mine + ((size_t)(c0 / 16) * 128 + row) * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            __stcg(dst + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
         }
       }
+      // the accumulator has been read: the MMAs of the next segment may start
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B.tempty + 8 * acc);
       if (++acc == 2) { acc = 0; aph ^= 1; }
+      if (whole) continue;
+      // stream-K segment: publish the partial sums, count this contribution
+      fence_acq_rel_gpu();
+      named_barrier_sync(kEpilogueThreads);
+      const long long t0 = (long long)ti * a.KT;
+      const int c_first = sk_cta_of(a, t0), c_last = sk_cta_of(a, t0 + a.KT - 1);
+      if (row == 0) *flag = atomicAdd(a.cnt + ti, 1u) == (unsigned)(c_last - c_first) ? 1u : 0u;
+      named_barrier_sync(kEpilogueThreads);
+      if (*flag) {
+        fence_acq_rel_gpu();  // acquire: every contributor's partial sums are visible
+        // CTAs after c_first start their range inside this tile (slot 0);
+        // c_first uses slot 0 only if its range starts at the tile's start
+        const size_t slot = (size_t)128 * a.BN;
+        const float* p0 = a.ws + ((size_t)c_first * 2 + (sk_begin(a, c_first) == t0 ? 0 : 1)) * slot;
+        const float* p1 = a.ws + (size_t)(c_first + 1) * 2 * slot;
+        const int others = c_last - c_first;
+#pragma unroll 1
+        for (int c0 = 0; c0 < a.BN; c0 += 16) {
+          const size_t off = ((size_t)(c0 / 16) * 128 + row) * 16;
+          // one 64-byte run per contributor: all its loads are issued together
+          float4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = __ldcg(reinterpret_cast<const float4*>(p0 + off) + j);
+#pragma unroll 1
+          for (int cc = 0; cc < others; ++cc) {
+            const float4* src = reinterpret_cast<const float4*>(p1 + (size_t)cc * 2 * slot + off);
+            float4 u[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) u[j] = __ldcg(src + j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[j].x += u[j].x; v[j].y += u[j].y; v[j].z += u[j].z; v[j].w += u[j].w;
+            }
+          }
+          if (n < a.N) {
+            const int m0 = mt * a.BN + c0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (m0 + 4 * j + e < a.M)
+                  a.y[(size_t)(m0 + 4 * j + e) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(vv[e]));
+            }
+          }
+        }
+        if (row == 0) a.cnt[ti] = 0u;
+      }
+      // every epilogue thread has read the flag before the next segment sets it
+      named_barrier_sync(kEpilogueThreads);
     }
   } else {
     // ---------------------------------------------------------------- dequant
@@ -246,8 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint32_t pph = 0;
     unsigned slab = (unsigned)h;  // this warp's slabs are h, h + 2, h + 4, ... of the CTA's stream
     bool ok = true;
-    for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-      for (int kt = 0; kt < a.KT && ok; ++kt) {
+    Sched sc = sched_begin(a);
+    Work wk;
+    while (ok && sched_next(a, sc, wk)) {
+      for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
         ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, kTimeoutNs);
         if (!ok) break;
         const uint8_t* pk = smem + (size_t)ps * a.tile_bytes;
@@ -313,9 +464,12 @@ struct GemmPlan {
   GemmArgs a;
   size_t smem;
   int grid;
+  size_t ws_bytes, cnt_bytes;  // stream-K workspace: partial sums, then arrival counters
 };
 
-int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
+// stream_k: split the tiles of the last, partial wave (plus one whole wave)
+// along K; needs the workspace sized by ws_bytes + cnt_bytes.
+int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
   GemmArgs& a = P->a;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = kSlabsPerTile * G.unit_bytes;
   a.BN = M >= 256 ? 256 : (M + 15) / 16 * 16;
@@ -337,7 +491,45 @@ int gemm_plan(const Geometry& G, int M, GemmPlan* P) {
   if (a.OPS == 0) return TF_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return TF_ERR_CUDA;
-  P->grid = a.ntiles < sms ? a.ntiles : sms;
+  const int rem = a.ntiles % sms;
+  // The last contributor to a split tile adds the others' partial sums one
+  // contributor after another, one L2 round trip (about 1 us) per 16 columns
+  // and contributor, so a split tile is shared by at most 2 CTAs (4 when
+  // BN <= 64).
+  const int split = a.BN <= 64 ? 4 : 2;
+  int sk = 0, sk_ctas = 1;
+  if (stream_k && rem != 0) {
+    if (a.ntiles > sms) {
+      // split the tiles of the partial wave only: every CTA still ends with
+      // whole tiles, behind whose MMAs the partial-sum additions are hidden
+      sk = rem;
+      sk_ctas = split * sk < sms ? split * sk : sms;
+    } else {
+      // every tile split: worth it when the k-iterations saved (about 1 us
+      // each, whatever BN is) exceed the addition left exposed at the end
+      const int ctas = split * a.ntiles < sms ? split * a.ntiles : sms;
+      const double c = (double)ctas / a.ntiles;
+      const double saved = a.KT * (1.0 - 1.0 / c);
+      if (saved >= a.BN / 16.0 * (c + 1.0) + 2.0) {
+        sk = a.ntiles;
+        sk_ctas = ctas;
+      }
+    }
+  }
+  if (sk > 0) {
+    a.dp_tiles = a.ntiles - sk;
+    // with fewer k-iterations than CTAs, one k-iteration each for the first ones
+    const long long iters = (long long)sk * a.KT;
+    a.sk_ctas = iters < sk_ctas ? (int)iters : sk_ctas;
+    P->grid = sms;
+    P->ws_bytes = (size_t)a.sk_ctas * 2 * 128 * a.BN * sizeof(float);
+    P->cnt_bytes = ((size_t)sk * sizeof(unsigned) + 255) / 256 * 256;
+  } else {
+    a.dp_tiles = a.ntiles;
+    a.sk_ctas = 1;
+    P->grid = a.ntiles < sms ? a.ntiles : sms;
+    P->ws_bytes = P->cnt_bytes = 0;
+  }
   return TF_OK;
 }
 
@@ -364,16 +556,32 @@ using namespace tf;
 
 extern "C" {
 
+int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes) {
+  if (!bytes) return TF_ERR_INVALID_ARG;
+  Geometry G;
+  int rc = make_geometry(N, K, bits, group, &G);
+  if (rc) return rc;
+  if (M < 1) return TF_ERR_INVALID_ARG;
+  GemmPlan P;
+  rc = gemm_plan(G, M, true, &P);
+  if (rc) return rc;
+  *bytes = P.ws_bytes + P.cnt_bytes;
+  return TF_OK;
+}
+
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x, uint16_t* y,
-            int M, cudaStream_t stream) {
+            int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   Geometry G;
   int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
   if (rc) return rc;
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y)) return TF_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace)) return TF_ERR_ALIGNMENT;
   GemmPlan P;
-  rc = gemm_plan(G, M, &P);
+  rc = gemm_plan(G, M, workspace != nullptr, &P);
   if (rc) return rc;
+  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes) return TF_ERR_WORKSPACE;
+  P.a.ws = static_cast<float*>(workspace);
+  P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
   P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   P.a.y = y;
   P.a.err = device_error_ptr();

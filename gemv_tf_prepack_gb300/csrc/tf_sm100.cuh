@@ -133,6 +133,26 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_cta(const void* p, unsigned
   return old;
 }
 
+// Named barrier 1 over `threads` threads (whole warps).
+__device__ __forceinline__ void named_barrier_sync(uint32_t threads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
+// Named barrier 1 over `threads` threads that also returns the AND of v over
+// them, so that the participants take the same branch afterwards.
+__device__ __forceinline__ bool named_barrier_and(uint32_t threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 // Wait until every cp.async this thread has issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 

@@ -141,14 +141,28 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
             cudaStream_t stream);
 
 /*
+ * Workspace bytes tf_gemm needs on the current device for this layer and M
+ * to split the K dimension of its last, partial wave of output tiles across
+ * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters.  0
+ * when the tiles fill whole waves.  Like the GEMV workspace it must be
+ * zero-filled before its first use, and every tf_gemm leaves it zero-filled.
+ */
+int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
+
+/*
  * Fused GEMM for prefill (Methodology 1: each weight tile is unpacked and
  * dequantised once into on-chip memory and reused for the tile's MMAs):
  * y[M, N] = x[M, K] * W^T for any M >= 1, with tcgen05 tensor-core MMAs
  * accumulating in tensor memory.  Device pointers: blob, x and y 16-byte
- * aligned.  No workspace.
+ * aligned.  With a workspace (16-byte aligned, >= tf_gemm_workspace_size)
+ * the output tiles of the last, partial wave are split along K across all
+ * SMs and their partial sums added in a fixed order (same result every run);
+ * with workspace NULL (workspace_bytes ignored) every tile is computed whole
+ * by one SM.  A workspace smaller than required gives TF_ERR_WORKSPACE.
  */
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
-            const uint16_t* x, uint16_t* y, int M, cudaStream_t stream);
+            const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
+            cudaStream_t stream);
 
 /*
  * tf_gemv without a caller-provided workspace, for callers that cannot

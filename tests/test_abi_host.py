@@ -123,7 +123,8 @@ def test_device_calls_validate_before_touching_the_gpu():
     # M out of range
     assert lib.tf_gemv(blob, size, 256, 512, 4, 128, x, y, 9, None, 0, None) == -2
     assert lib.tf_gemv(blob, size, 256, 512, 4, 128, x, y, 0, None, 0, None) == -1
-    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 0, None) == -1
-    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, ctypes.c_void_p(8194), y, 4, None) == -3
+    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 0, None, 0, None) == -1
+    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, ctypes.c_void_p(8194), y, 4, None, 0, None) == -3
+    assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 4, ctypes.c_void_p(8200), 64, None) == -3
     assert lib.tf_dequant(None, size, 256, 512, 4, 128, y, None) == -1
     assert lib.tf_dequant(blob, size, 256, 512, 4, 96, y, None) == -2

@@ -168,3 +168,33 @@ def test_gemv_slab_long_k(N, K, bits, group, M):
                                      np.random.default_rng(0).integers(0, N, 64)]))
     ref = tf_oracle.reference_rows(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb, rows)
     check_close(y[:, rows], ref, f"long-K slab gemv {N}x{K} w{bits} g{group} M={M}")
+
+
+# Shapes whose tiles the GEMM splits along K on a 152-SM GB300: a partial wave
+# over more than one wave of tiles (N = 20480 and 19712 rows, a ragged
+# N = 20000 with a ragged K), and every tile split when there are few tiles
+# (M = 37 over 3 tiles; M = 1 over 2 tiles with 32 k-iterations each, so
+# 32 CTAs add into one tile).
+STREAM_K = [
+    (20480, 384, 4, 128, 16), (19712, 2048, 4, 128, 300), (20000, 1016, 4, 0, 40),
+    (384, 4096, 8, 64, 37), (256, 4096, 8, 0, 1), (2048, 1536, 4, 128, 512),
+]
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", STREAM_K)
+def test_gemm_stream_k_and_whole_tiles(N, K, bits, group, M):
+    """Both GEMM schedules against the oracle: output tiles split along K across
+    SMs (partial sums added in a fixed order), and every tile whole on one SM."""
+    import torch
+    qw, W = layer(N, K, bits, group, 39)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152 and (N, M) != (2048, 512):
+        assert tf.gemm_workspace_size(N, K, bits, group, M) > 0, "expected a K-split schedule"
+    xb = synth.make_activations(M, K, 39, outliers=True)
+    x = to_dev_bf16(xb)
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
+    y_sk = to_host_bits(tf.gemm(W, x))
+    y_dp = to_host_bits(tf.gemm(W, x, stream_k=False))
+    check_close(y_sk, ref, f"stream-K gemm {N}x{K} M={M}")
+    check_close(y_dp, ref, f"whole-tile gemm {N}x{K} M={M}")
+    np.testing.assert_array_equal(y_sk, to_host_bits(tf.gemm(W, x)))  # same sums every run
+    assert tf.device_error() == 0
