@@ -598,15 +598,21 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
     mbar_init_fence();
   }
   __syncthreads();
+  // Static weights start streaming before the grid dependency resolves.
+  // With resident activations only the first stage does: the activation
+  // copies issued at the dependency would otherwise reach the SM behind
+  // every prefetched stage; the other stages follow them.
+  const int npre_w = XRES ? (npre < 1 ? npre : 1) : npre;
   if (warp == 0) {
     if (lane == 0) griddep_launch_dependents();
-    // static weights first, before the grid dependency resolves
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
+    for (int f = 0; f < npre_w; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
   }
   // y and x may still be in use by the previous grid
   griddep_wait();
   if (XRES) {
     copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, NW * 32);
+    if (warp == 0)
+      for (int f = npre_w; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
     cp_async_wait_all();
     __syncthreads();
   } else if (warp == 0) {
