@@ -118,9 +118,11 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
 
 /*
  * Workspace bytes tf_gemv needs on the current device for this layer and M
- * (split-K partial sums plus per-block arrival counters).  The workspace must
- * be zero-filled before its first use; every tf_gemv leaves it zero-filled
- * again, so one workspace can be reused by calls ordered on one stream.
+ * (split-K partial sums plus per-block arrival counters; 0 for layers whose
+ * blocks each stream whole 16-row slabs).  The workspace must be
+ * zero-filled before its first use; every tf_gemv leaves the arrival
+ * counters at zero again (the partial sums are always written before they
+ * are read), so one workspace can be reused by calls ordered on one stream.
  */
 int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
