@@ -6,8 +6,10 @@
 // tokens (BN <= 256):
 //   warp 0       streams pre-tiled weight tiles (one 3-D TMA box: the eight
 //                16-row units of the tile, each carrying its own scales and
-//                zeros) and the matching activation slabs (2-D TMA, 128-byte
-//                swizzle) into shared-memory rings;
+//                zeros) into a shared-memory ring;
+//   warp 22      streams the matching activation slabs (2-D TMA, 128-byte
+//                swizzle) into the operand ring, next to where the dequant
+//                warps put the weights;
 //   warps 6..21  unpack + dequantise one (16-row block, 64-column slab) of
 //                each tile into the UMMA K-major 128-byte-swizzled layout
 //                (bit-exact bf16_rne((q - z) * s));
@@ -36,7 +38,8 @@ namespace tf {
 
 namespace {
 
-constexpr int kThreads = 704;        // 22 warps
+constexpr int kThreads = 736;        // 23 warps
+constexpr int kXProducerWarp = 22;   // the activation slabs' producer
 constexpr int kDequantWarp0 = 6;     // warps 6..21: (row block, slab) pairs
 constexpr int kEpilogueWarp0 = 2;    // warps 2..5
 constexpr int kEpilogueThreads = 128;
@@ -190,15 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + (B.tmem_slot - sbase));
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------- weight producer
     if (lane == 0) {
-      int ps = 0, os = 0;
-      uint32_t pph = 0, oph = 0;
+      int ps = 0;
+      uint32_t pph = 0;
       bool ok = true;
       Sched sc = sched_begin(a);
       Work wk;
       while (ok && sched_next(a, sc, wk)) {
-        const int nb = wk.tile / a.MT, mt = wk.tile - nb * a.MT;
+        const int nb = wk.tile / a.MT;
         for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
           ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
           if (!ok) break;
@@ -209,6 +212,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           else
             tma_load_4d(dst, &tmw, 0, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
           if (++ps == a.P) { ps = 0; pph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == kXProducerWarp) {
+    // ------------------------------------------------------- activation producer
+    // The x slabs have their own producer, so that the packed weight tiles
+    // are requested as far ahead as the packed ring allows rather than only
+    // as far as the operand ring.
+    if (lane == 0) {
+      int os = 0;
+      uint32_t oph = 0;
+      bool ok = true;
+      Sched sc = sched_begin(a);
+      Work wk;
+      while (ok && sched_next(a, sc, wk)) {
+        const int mt = wk.tile % a.MT;
+        for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
           for (int h = 0; h < 2; ++h) {
             ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
             if (!ok) break;
