@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 
 #include "../../include/tf.h"
 #include "tf_abi.h"
@@ -46,6 +47,9 @@ constexpr int kEpilogueThreads = 128;
 constexpr int kSlabBytesW = 128 * 128;  // 128 rows x 64 BF16
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr uint64_t kTimeoutNs = 4000000000ull;
+// Epilogue staging: two buffers of 16 tokens x 128 rows of BF16 (one TMA box each).
+constexpr int kEpiChunk = 16;
+constexpr int kEpiStageBytes = 2 * kEpiChunk * kTileN * 2;
 
 enum : unsigned {
   kErrProducerWait = 0x100,
@@ -66,7 +70,8 @@ struct GemmArgs {
   int dp_tiles;               // tiles [0, dp_tiles) whole per CTA; the rest split along K
   int sk_ctas;                // CTAs [0, sk_ctas) share the split tiles' k-iterations (at least one each)
   int P, OPS;                 // stages of the packed ring and of the operand ring
-  int off_op, off_bar;        // byte offsets in the 1024-aligned dynamic smem
+  int y_tma;                  // 1: whole tiles leave through shared-memory staging and TMA stores
+  int off_op, off_epi, off_bar;  // byte offsets in the 1024-aligned dynamic smem
 };
 
 struct Bars {
@@ -155,6 +160,7 @@ __device__ __forceinline__ Bars bars_at(uint32_t base, int P, int OPS) {
 template <int BITS, int GPT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmx,
                                                            const __grid_constant__ CUtensorMap tmw,
+                                                           const __grid_constant__ CUtensorMap tmy,
                                                            const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     mbar_init_fence();
     prefetch_tensormap(&tmx);
     prefetch_tensormap(&tmw);
+    if (a.y_tma) prefetch_tensormap(&tmy);
   }
   if (warp == 1) {
     tmem_alloc(B.tmem_slot, kTmemCols);
@@ -312,7 +319,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         uint32_t r[16];
         tmem_ld_16(taddr + (uint32_t)c0, r);
         tmem_ld_wait();
-        if (whole) {
+        if (whole && a.y_tma) {
+          // Stage the chunk (16 tokens x 128 rows, BF16, [token][row]) and
+          // write it with one TMA box; rows past N and tokens past M are
+          // left out by the tensor map.  Two buffers: before one is
+          // overwritten, the store that read it two chunks ago has finished
+          // reading.
+          if (mt * a.BN + c0 < a.M) {
+            const int buf = (c0 / kEpiChunk) & 1;
+            if (row == 0) bulk_wait_group_read<1>();
+            named_barrier_sync(kEpilogueThreads);
+            uint16_t* stg = reinterpret_cast<uint16_t*>(smem + a.off_epi) + buf * (kEpiChunk * kTileN);
+#pragma unroll
+            for (int j = 0; j < kEpiChunk; ++j)
+              stg[j * kTileN + row] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+            fence_async_shared();
+            named_barrier_sync(kEpilogueThreads);
+            if (row == 0) {
+              tma_store_2d(&tmy, smem_u32(stg), nb * kTileN, mt * a.BN + c0);
+              bulk_commit_group();
+            }
+          }
+        } else if (whole) {
           const int m0 = mt * a.BN + c0;
           if (n < a.N) {
 #pragma unroll
@@ -386,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // every epilogue thread has read the flag before the next segment sets it
       named_barrier_sync(kEpilogueThreads);
     }
+    // the staged tiles' stores must be done reading shared memory (and
+    // writing y) before the CTA ends
+    if (row == 0) bulk_wait_group_all();
   } else {
     // ---------------------------------------------------------------- dequant
     // Warp (mb, h): unit mb (rows 16 mb .. 16 mb + 15) and 64-column slab h
@@ -414,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     int ps = 0;
     uint32_t pph = 0;
     unsigned slab = (unsigned)h;  // this warp's slabs are h, h + 2, h + 4, ... of the CTA's stream
+    // A stage's proxy fence and full-barrier arrive are deferred until the
+    // next k-step's tile has been unpacked and dequantised, so that the
+    // fence's wait for the stores overlaps that work.
+    int pend = -1;
     bool ok = true;
     Sched sc = sched_begin(a);
     Work wk;
@@ -452,6 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(B.empty_p + 8 * ps);
         if (++ps == a.P) { ps = 0; pph ^= 1; }
+        if (pend >= 0) {
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.full_op + 8 * pend);
+          pend = -1;
+        }
         const unsigned os = slab % (unsigned)a.OPS;
         const uint32_t oph = (slab / (unsigned)a.OPS) & 1u;
         ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, kTimeoutNs);
@@ -461,11 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         *reinterpret_cast<uint4*>(wsl + dst[0][1]) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         *reinterpret_cast<uint4*>(wsl + dst[1][0]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(wsl + dst[1][1]) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(B.full_op + 8 * os);
+        pend = (int)os;
         slab += 2;
       }
+    }
+    if (pend >= 0) {
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.full_op + 8 * pend);
     }
   }
 
@@ -496,14 +540,18 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
   a.MT = (M + a.BN - 1) / a.BN;
   a.ntiles = G.NB * a.MT;
   const int op_stage = kSlabBytesW + a.BN * 128;
+  // y as a TMA tensor needs rows of a multiple of 16 bytes
+  a.y_tma = G.N % 8 == 0 ? 1 : 0;
+  const int epi = a.y_tma ? kEpiStageBytes : 0;
   a.OPS = 0;
   for (int ops = 4; ops >= 2 && a.OPS == 0; --ops)
     for (int p = 4; p >= 2; --p) {
       const int off_op = (p * a.tile_bytes + 1023) / 1024 * 1024;
-      const int off_bar = off_op + ops * op_stage;
+      const int off_epi = off_op + ops * op_stage;
+      const int off_bar = off_epi + epi;
       const size_t smem = 1024 + off_bar + 256;
       if (smem <= (size_t)kMaxSmem) {
-        a.P = p; a.OPS = ops; a.off_op = off_op; a.off_bar = off_bar;
+        a.P = p; a.OPS = ops; a.off_op = off_op; a.off_epi = off_epi; a.off_bar = off_bar;
         P->smem = smem;
         break;
       }
@@ -554,7 +602,8 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
 }
 
 template <int BITS, int GPT>
-int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const GemmPlan& P, cudaStream_t s) {
+int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorMap& ymap, const GemmPlan& P,
+                cudaStream_t s) {
   auto kfn = gemm_kernel<BITS, GPT>;
   // Opt in once per device to the largest shared-memory carve-out.
   static std::atomic<unsigned long long> opted{0};
@@ -565,7 +614,7 @@ int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const GemmPlan&
       return TF_ERR_CUDA;
     opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }
-  kfn<<<P.grid, kThreads, P.smem, s>>>(map, wmap, P.a);
+  kfn<<<P.grid, kThreads, P.smem, s>>>(map, wmap, ymap, P.a);
   return launch_status();
 }
 
@@ -606,19 +655,25 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   P.a.y = y;
   P.a.err = device_error_ptr();
   if (!P.a.err) return TF_ERR_CUDA;
-  CUtensorMap map, wmap;
+  CUtensorMap map, wmap, ymap;
   rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
   if (rc) return rc;
   rc = encode_units_map(P.a.units, G.S, G.KT, G.unit_bytes, &wmap);
   if (rc) return rc;
-  if (bits == 4) {
-    if (G.gpt == 1) return launch_gemm<4, 1>(map, wmap, P, stream);
-    if (G.gpt == 2) return launch_gemm<4, 2>(map, wmap, P, stream);
-    return launch_gemm<4, 4>(map, wmap, P, stream);
+  if (P.a.y_tma) {
+    rc = encode_y_map(y, M, N, &ymap);
+    if (rc) return rc;
+  } else {
+    memset(&ymap, 0, sizeof(ymap));  // not read by the kernel
   }
-  if (G.gpt == 1) return launch_gemm<8, 1>(map, wmap, P, stream);
-  if (G.gpt == 2) return launch_gemm<8, 2>(map, wmap, P, stream);
-  return launch_gemm<8, 4>(map, wmap, P, stream);
+  if (bits == 4) {
+    if (G.gpt == 1) return launch_gemm<4, 1>(map, wmap, ymap, P, stream);
+    if (G.gpt == 2) return launch_gemm<4, 2>(map, wmap, ymap, P, stream);
+    return launch_gemm<4, 4>(map, wmap, ymap, P, stream);
+  }
+  if (G.gpt == 1) return launch_gemm<8, 1>(map, wmap, ymap, P, stream);
+  if (G.gpt == 2) return launch_gemm<8, 2>(map, wmap, ymap, P, stream);
+  return launch_gemm<8, 4>(map, wmap, ymap, P, stream);
 }
 
 }  // extern "C"

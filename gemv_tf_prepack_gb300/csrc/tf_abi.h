@@ -21,6 +21,9 @@ unsigned* device_error_ptr();
 // columns x `rows` rows with the 128-byte swizzle (one GEMM operand slab).
 int encode_x_map(const uint16_t* x, int M, int K, CUtensorMap* map);
 int encode_x_map_sw128(const uint16_t* x, int M, int K, int rows, CUtensorMap* map);
+// encode_y_map: the output y [M, N] BF16 (N a multiple of 8) as a 2-D map
+// with a box of 128 columns (N) x 16 rows (M), for tile stores.
+int encode_y_map(const uint16_t* y, int M, int N, CUtensorMap* map);
 
 // TMA map over the S x KT units of a blob (8-byte elements): one box is the
 // eight units of a 128-row tile at one kt, written densely (unit after unit)

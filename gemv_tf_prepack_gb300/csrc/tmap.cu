@@ -48,6 +48,9 @@ int encode_x_map(const uint16_t* x, int M, int K, CUtensorMap* map) {
   return encode(x, M, K, kTileK, (unsigned)M, CU_TENSOR_MAP_SWIZZLE_NONE, map);
 }
 
+int encode_y_map(const uint16_t* y, int M, int N, CUtensorMap* map) {
+  return encode(y, M, N, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE, map);
+}
 int encode_x_map_sw128(const uint16_t* x, int M, int K, int rows, CUtensorMap* map) {
   return encode(x, M, K, 64, (unsigned)rows, CU_TENSOR_MAP_SWIZZLE_128B, map);
 }
