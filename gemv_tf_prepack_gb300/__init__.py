@@ -166,13 +166,36 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    return (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+
+
+def _workspace_args(W, M: int, kind: str, workspace):
+    """(device address, bytes) of the given workspace, else of the layer's cached one."""
+    if workspace is not None:
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    args = W._ws_args.get((kind, M))
+    if args is None:
+        ws = W.workspace(M, kind)
+        args = W._ws_args[(kind, M)] = (ws.data_ptr(), ws.numel() * ws.element_size())
+    return args
+
+
 class Weights:
-    """A device-resident blob plus its layer description."""
+    """A device-resident blob plus its layer description.
+
+    The blob tensor is fixed at construction: its device address is kept for
+    the calls, so replace the Weights object rather than its `blob`.
+    """
 
     def __init__(self, blob_dev, N: int, K: int, bits: int, group: int):
         self.blob = blob_dev
         self.N, self.K, self.bits, self.group = N, K, bits, group
         self._ws = {}
+        self._ws_args = {}  # (kind, M) -> (device address, bytes) of the cached workspace
+        self._blob_ptr = blob_dev.data_ptr()
+        self._blob_bytes = blob_dev.numel()
 
     @classmethod
     def upload(cls, blob: np.ndarray, device=None) -> "Weights":
@@ -236,9 +259,9 @@ def gemv(W: Weights, x, y=None, workspace=None, stream=None):
     _check_x(W, x)
     M = x.shape[0]
     y = _out(W, M, y)
-    ws = W.workspace(M) if workspace is None else workspace
-    _check(_lib().tf_gemv(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
-                          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "tf_gemv")
+    wp, wn = _workspace_args(W, M, "gemv", workspace)
+    _check(_lib().tf_gemv(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(), M,
+                          wp, wn, _stream_handle(stream)), "tf_gemv")
     return y
 
 
@@ -273,12 +296,11 @@ def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True):
     M = x.shape[0]
     y = _out(W, M, y)
     if stream_k:
-        ws = W.workspace(M, "gemm") if workspace is None else workspace
-        wp, wn = _ptr(ws), ws.numel() * ws.element_size()
+        wp, wn = _workspace_args(W, M, "gemm", workspace)
     else:
         wp, wn = None, 0
-    _check(_lib().tf_gemm(_ptr(W.blob), W.nbytes, W.N, W.K, W.bits, W.group, _ptr(x), _ptr(y), M,
-                          wp, wn, _stream(stream)), "tf_gemm")
+    _check(_lib().tf_gemm(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(), M,
+                          wp, wn, _stream_handle(stream)), "tf_gemm")
     return y
 
 
