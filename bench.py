@@ -208,6 +208,29 @@ def launch_times(torch, ev, ncopies, layers, fn, stream):
     return out
 
 
+def rank_barrier(world: int):
+    """Barrier over all ranks (a no-op on one)."""
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def rank_max(v: float, world: int, device: str = "cuda") -> float:
+    """The maximum of v over all ranks (timings: the slowest rank sets the job's time)."""
+    if world == 1:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput of N independent replicas (weak scaling): every
+    rank's units over the slowest rank's time, per second."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -220,15 +243,10 @@ def run_ours(args, rank, world):
     stream = torch.cuda.Stream()
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(v, world)
 
     # ---------------- decode GEMV step (headline value) ----------------
     step_bytes = sum(algo_bytes(1, N, K) for N, K, _ in DECODE)
@@ -269,7 +287,7 @@ def run_ours(args, rank, world):
     kernel_ms = ms_step / len(DECODE)
     per_launch_bytes = step_bytes / len(DECODE)
     achieved = per_launch_bytes / (kernel_ms * 1e-3) / 1e9
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_rate(step_bytes, world, ms_step) / 1e9
     # For reference: each launch alone, bracketed by events captured in a graph
     # (no overlap with its neighbours), after the timed region.
     iso_graphs = [capture_step(torch, gemv_call, dec, r, stream, ev[r]) for r in range(copies)]
@@ -311,7 +329,7 @@ def run_ours(args, rank, world):
             y_pin.copy_(y_dev[r], non_blocking=True)
             stream.synchronize()
     e2e_ms = max_over_ranks((time.perf_counter() - te) * 1e3 / e2e_steps)
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
 
     # ---------------- prefill GEMM (M=2048) ----------------
     for L in dec:
@@ -356,7 +374,7 @@ def run_ours(args, rank, world):
     p_iso_us = {f"{N}x{K}": round(1e3 * sum(pk[r * len(PREFILL) + i] for r in range(pcopies)) / pcopies, 1)
                 for i, (N, K, _) in enumerate(PREFILL)}
     p_achieved = flops / len(PREFILL) / (p_kernel_ms * 1e-3) / 1e12
-    prefill_tflops = world * flops / (pms * 1e-3) / 1e12
+    prefill_tflops = job_rate(flops, world, pms) / 1e12
     long_region = pms * psteps > 1000.0
     tc_ref = tc_peak_sus if long_region else tc_peak
     pclocks = pclk.summary()
