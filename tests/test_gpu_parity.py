@@ -198,3 +198,39 @@ def test_gemm_stream_k_and_whole_tiles(N, K, bits, group, M):
     check_close(y_dp, ref, f"whole-tile gemm {N}x{K} M={M}")
     np.testing.assert_array_equal(y_sk, to_host_bits(tf.gemm(W, x)))  # same sums every run
     assert tf.device_error() == 0
+
+
+def _random_layers(n, seed):
+    """Seeded random layer shapes: INT4/INT8, every group kind, ragged N and K, M from 1 to ~700."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        bits = int(rng.choice([4, 8]))
+        group = int(rng.choice([0, 32, 64, 128, 256]))
+        if group == 0:
+            K = int(rng.integers(1, 600)) * 8
+        elif group == 256:
+            K = int(rng.integers(1, 20)) * 256
+        else:
+            K = int(rng.integers(1, 40)) * group
+        N = int(rng.integers(1, 6000))
+        if N * K > 12_000_000:
+            N = max(1, 12_000_000 // K)
+        M = int(rng.choice([int(rng.integers(1, 9)), int(rng.integers(9, 80)), int(rng.integers(80, 700))]))
+        out.append((N, K, bits, group, M))
+    return out
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", _random_layers(16, 2027))
+def test_random_layers(N, K, bits, group, M):
+    """GEMM (whole tiles or stream-K, TMA or element stores) and, at M <= 8, GEMV on random shapes."""
+    qw, W = layer(N, K, bits, group, 43)
+    xb = synth.make_activations(M, K, 43, outliers=True)
+    x = to_dev_bf16(xb)
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
+    y = to_host_bits(tf.gemm(W, x))
+    check_close(y, ref, f"gemm {N}x{K} w{bits} g{group} M={M}")
+    np.testing.assert_array_equal(y, to_host_bits(tf.gemm(W, x)))
+    if M <= 8:
+        check_close(to_host_bits(tf.gemv(W, x)), ref, f"gemv {N}x{K} w{bits} g{group} M={M}")
+    assert tf.device_error() == 0
