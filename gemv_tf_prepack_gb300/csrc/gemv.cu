@@ -796,13 +796,15 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
     P->x_res = slab_ring(P, M, (U8 * Gm.unit_bytes + 127) / 128 * 128, xres, 2, kGemvSmemBudget) >= 2;
     if (P->x_res) return TF_OK;
     // (2) x too large for that: sixteen warps, one CTA per SM, x resident
-    // next to a ring of up to four stages.
+    // next to a ring of two to four stages.  Two stages still beat x slices
+    // travelling with every stage, which each CTA re-reads from L2 for every
+    // slab (INT8 8192 x 8192 at M = 8: 25 us against 44 us).
     P->nw = 16;
     P->spc = (nslab + sms - 1) / sms;
     P->G = (nslab + P->spc - 1) / P->spc;
     const int U16 = 16 * slab_units_per_warp(Gm.bits, true, 16);
     P->QPS = (Gm.KT + U16 - 1) / U16;
-    P->x_res = slab_ring(P, M, (U16 * Gm.unit_bytes + 127) / 128 * 128, xres, 4, kGemvSmemMax1 - 128) >= 3;
+    P->x_res = slab_ring(P, M, (U16 * Gm.unit_bytes + 127) / 128 * 128, xres, 4, kGemvSmemMax1 - 128) >= 2;
     if (P->x_res) return TF_OK;
     // (3) Eight warps, two CTAs per SM, x slices travelling with each stage.
     P->nw = 8;

@@ -151,10 +151,13 @@ def test_gemm_even_blocks(N, K, bits, group, M):
 
 
 # Long K: x no longer fits next to a ring at two CTAs per SM, so the slab GEMV
-# runs sixteen warps per CTA with x resident (the first three), or carries x
-# with every stage (M = 8).  Sampled output rows: the oracle row by row.
+# runs sixteen warps per CTA with x resident (the first three and the last
+# two, those with a ring of only two stages), or carries x with every stage
+# (M = 8 at K = 16384).  Sampled output rows: the oracle row by row.
 LONG_K = [
     (2440, 24576, 4, 32, 1), (2432, 16384, 8, 64, 2), (2432, 32768, 4, 128, 1), (2440, 16384, 4, 128, 8),
+    # 128 KB of resident x next to a two-stage ring
+    (2440, 8192, 8, 0, 8), (2440, 16384, 4, 128, 4),
 ]
 
 
