@@ -480,24 +480,23 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 // slab GEMV (whole slabs per CTA, K split across the CTA's warps)
 //
 // CTA c owns slabs [c*spc, min((c+1)*spc, nslab)) — one contiguous byte
-// range of the blob — over all of K.  Its ring stage holds U = 8*UPW
-// consecutive units of one slab (one bulk copy).  The activations are
-// copied with 16-byte cp.async (load/store path, so they do not queue behind
-// weight copies already issued to the TMA unit): all of x once, into a
-// resident buffer, when it fits, else each stage's slices with the stage.
-// A CTA has eight warps (two CTAs per SM) or, when x is too large to stay
-// resident next to a useful ring at two CTAs per SM, sixteen (one per SM).
+// range of the blob — over all of K.  Its ring stage holds U = NW*UPW
+// consecutive units of one slab (one bulk copy).  All of x is copied once,
+// into a resident buffer, with 16-byte cp.async (load/store path, so it does
+// not queue behind weight copies already issued to the TMA unit).  A CTA has
+// eight warps (two CTAs per SM) or, when x is too large to stay resident
+// next to a ring at two CTAs per SM, sixteen (one per SM).  Layers whose x
+// does not fit even then take the tile GEMV.
 // Warp w takes units w, w + NW, ... of every stage.  At the end of a slab
 // each warp parks its partial sums in its own shared-memory slot and goes
 // on; after the last slab the eight warps add the CTA's slabs in parallel
 // (each slab's eight partials in warp order) and write y, so no warp waits
 // for another inside the stream.
 
-// Units per warp per ring stage.  With resident activations a stage of the
-// eight-warp configuration holds only weights, so it can be twice as large
-// (fewer handovers per unit).
-__host__ __device__ constexpr int slab_units_per_warp(int bits, bool xres, int nw) {
-  return (bits == 4 ? 2 : 1) * (xres && nw == 8 ? 2 : 1);
+// Units per warp per ring stage (the eight-warp configuration's stages are
+// twice as large: fewer handovers per unit).
+__host__ __device__ constexpr int slab_units_per_warp(int bits, int nw) {
+  return (bits == 4 ? 2 : 1) * (nw == 8 ? 2 : 1);
 }
 
 struct SlabArgs {
@@ -507,19 +506,17 @@ struct SlabArgs {
   unsigned* err;
   int N, K, M, KT, g;
   int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
-  int x_res;            // 1: x resident in shared memory; 0: x slices travel with each stage
-  int NS, stage_bytes, x_off, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
+  int NS, stage_bytes, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
 };
 
-// 16-byte chunks r in [r0, r1) (stepping by `step`) of the activation columns
-// [128*k0, 128*(k0 + n)) for every token, into [unit][token][128] at dst;
-// columns past K are zero-filled.
-__device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int k0, int n, int r0, int step) {
-  const int per_m = n * 16;
+// 16-byte chunks r = r0, r0 + step, ... of the activations x[M, K], into
+// [unit][token][128] at dst; columns past K are zero-filled.
+__device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int r0, int step) {
+  const int per_m = a.KT * 16;
   for (int m = 0; m < a.M; ++m) {
     const uint16_t* xm = a.x + (size_t)m * a.K;
     for (int r = r0; r < per_m; r += step) {
-      const int col = (k0 * kTileK) + 8 * r;
+      const int col = 8 * r;
       const bool in = col < a.K;
       cp_async_16(dst + (uint32_t)((r >> 4) * a.M * 256 + m * 256 + (r & 15) * 16), xm + (in ? col : 0),
                   in ? 16u : 0u);
@@ -528,34 +525,27 @@ __device__ __forceinline__ void copy_x(const SlabArgs& a, uint32_t dst, int k0, 
 }
 
 // Fill f of the CTA whose first slab is s0: units [U*q, U*q + n) of slab
-// s0 + f / QPS (q = f % QPS) into stage st.  Weights: one bulk copy issued
-// by lane 0.  Per-stage activations (x_res == 0): all 32 lanes copy 16-byte
-// chunks and each lane then arrives on the stage's barrier once its copies
-// have landed (the barrier then expects 1 + 32 arrivals per fill).
-template <int BITS, int GPT, bool XRES, int NW>
+// s0 + f / QPS (q = f % QPS) into stage st, as one bulk copy issued by lane 0.
+template <int BITS, int GPT, int NW>
 __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uint32_t full, int s0, int f, int st,
-                                          bool weights, bool x, int lane) {
+                                          int lane) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int U = NW * slab_units_per_warp(BITS, XRES, NW);
+  constexpr int U = NW * slab_units_per_warp(BITS, NW);
   const int qs = f / a.QPS;
   const int sl = s0 + qs, k0 = (f - qs * a.QPS) * U;
   const int n = a.KT - k0 < U ? a.KT - k0 : U;
   const uint32_t bar = full + 8u * st;
   const uint32_t dst = sbase + (uint32_t)(st * a.stage_bytes);
-  if (weights && lane == 0) {
+  if (lane == 0) {
     mbar_arrive_expect_tx(bar, (uint32_t)(n * UB));
     bulk_load(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar);
-  }
-  if (x && !XRES) {
-    copy_x(a, dst + (uint32_t)a.x_off, k0, n, lane, 32);
-    cp_async_mbar_arrive_noinc(bar);
   }
 }
 
 // Hand stage st (fill f) back; the last warp to do so refills it with fill
 // f + NS.  The release counter's acquire-release atomic orders every warp's
 // reads of the stage before the refill that overwrites it.
-template <int BITS, int GPT, bool XRES, int NW>
+template <int BITS, int GPT, int NW>
 __device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbase, uint32_t full, unsigned* released,
                                                 int* ctl, int s0, int f, int st, int nfill, bool dead, int lane) {
   __syncwarp();
@@ -565,15 +555,15 @@ __device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbas
     refill = !dead && f + a.NS < nfill;
     if (refill) atomicAdd(ctl, 1);
   }
-  if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f + a.NS, st, true, true, lane);
+  if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, NW>(a, sbase, full, s0, f + a.NS, st, lane);
 }
 
-template <int BITS, int GPT, bool XRES, int NW>
+template <int BITS, int GPT, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(const SlabArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align128(smem_raw);
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int UPW = slab_units_per_warp(BITS, XRES, NW);
+  constexpr int UPW = slab_units_per_warp(BITS, NW);
   constexpr int U = NW * UPW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t = lane & 3;
@@ -590,7 +580,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
   const int npre = nfill < a.NS ? nfill : a.NS;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.NS; ++i) {
-      mbar_init(full + 8 * i, XRES ? 1 : 1 + 32);
+      mbar_init(full + 8 * i, 1);
       released[i] = 0;
     }
     ctl[0] = npre;
@@ -598,31 +588,26 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
     mbar_init_fence();
   }
   __syncthreads();
-  // Static weights start streaming before the grid dependency resolves.
-  // With resident activations only the first stage does: the activation
-  // copies issued at the dependency would otherwise reach the SM behind
-  // every prefetched stage; the other stages follow them.
-  const int npre_w = XRES ? (npre < 1 ? npre : 1) : npre;
+  // Static weights start streaming before the grid dependency resolves, but
+  // only the first stage: the activation copies issued at the dependency
+  // would otherwise reach the SM behind every prefetched stage; the other
+  // stages follow them.
   if (warp == 0) {
     if (lane == 0) griddep_launch_dependents();
-    for (int f = 0; f < npre_w; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
+    if (npre > 0) slab_fill<BITS, GPT, NW>(a, sbase, full, s0, 0, 0, lane);
   }
   // y and x may still be in use by the previous grid
   griddep_wait();
-  if (XRES) {
-    copy_x(a, sbase + (uint32_t)a.xres_off, 0, a.KT, threadIdx.x, NW * 32);
-    if (warp == 0)
-      for (int f = npre_w; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, true, false, lane);
-    cp_async_wait_all();
-    __syncthreads();
-  } else if (warp == 0) {
-    for (int f = 0; f < npre; ++f) slab_fill<BITS, GPT, XRES, NW>(a, sbase, full, s0, f, f, false, true, lane);
-  }
+  copy_x(a, sbase + (uint32_t)a.xres_off, threadIdx.x, NW * 32);
+  if (warp == 0)
+    for (int f = 1; f < npre; ++f) slab_fill<BITS, GPT, NW>(a, sbase, full, s0, f, f, lane);
+  cp_async_wait_all();
+  __syncthreads();
 
   const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
   const int x_unit = a.M * 256;
-  // This warp's units of a stage are w, w + 8, ...: their offsets in the
-  // stage and in the stage's activation slices.
+  // This warp's units of a stage are w, w + NW, ...: their offsets in the
+  // stage and in the resident activations (from the stage's first unit).
   int woff[UPW], xoff[UPW];
 #pragma unroll
   for (int j = 0; j < UPW; ++j) {
@@ -642,16 +627,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
     const bool whole = q < a.QPS - 1 || last_n == U;  // every warp has UPW units in this stage
     const int n = whole ? U : last_n;
     if (!dead && !warp_wait(full + 8 * st, lap & 1u, a.err)) dead = true;
-    const uint8_t* xp = XRES ? xq : stp + a.x_off;
+    const uint8_t* xp = xq;
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j)
         if (whole || j * NW + warp < n) load_w(R[j], stp + woff[j], o);
     }
-    // With resident activations the stage is handed back as soon as its
-    // weights are in registers; per-stage activations are read right before
-    // their MMAs, so that stage goes back after them.
-    if (XRES) hand_back_stage<BITS, GPT, XRES, NW>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
+    // The stage goes back as soon as its weights are in registers.
+    hand_back_stage<BITS, GPT, NW>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (!dead) {
 #pragma unroll
       for (int j = 0; j < UPW; ++j) {
@@ -665,7 +648,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
         }
       }
     }
-    if (!XRES) hand_back_stage<BITS, GPT, XRES, NW>(a, sbase, full, released, ctl, s0, f, st, nfill, dead, lane);
     if (++q == a.QPS) {
       // Slab s0 + si is done for this warp: park its partial sums (only
       // lanes t < tq hold real tokens); the slabs are reduced after the loop.
@@ -747,7 +729,7 @@ struct GemvPlan {
   size_t partial_bytes, counter_bytes;
   // slab GEMV
   int nw;  // warps per CTA: 8 (two CTAs per SM) or 16 (one CTA per SM)
-  int nslab, spc, QPS, x_res, xres_off, red_off, ctl_off;
+  int nslab, spc, QPS, xres_off, red_off, ctl_off;
   size_t smem;
 };
 
@@ -791,30 +773,22 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
     P->nw = 8;
     P->spc = (nslab + 2 * sms - 1) / (2 * sms);
     P->G = (nslab + P->spc - 1) / P->spc;
-    const int U8 = 8 * slab_units_per_warp(Gm.bits, true, 8);
+    const int U8 = 8 * slab_units_per_warp(Gm.bits, 8);
     P->QPS = (Gm.KT + U8 - 1) / U8;
-    P->x_res = slab_ring(P, M, (U8 * Gm.unit_bytes + 127) / 128 * 128, xres, 2, kGemvSmemBudget) >= 2;
-    if (P->x_res) return TF_OK;
+    if (slab_ring(P, M, (U8 * Gm.unit_bytes + 127) / 128 * 128, xres, 2, kGemvSmemBudget) >= 2) return TF_OK;
     // (2) x too large for that: sixteen warps, one CTA per SM, x resident
-    // next to a ring of two to four stages.  Two stages still beat x slices
-    // travelling with every stage, which each CTA re-reads from L2 for every
-    // slab (INT8 8192 x 8192 at M = 8: 25 us against 44 us).
+    // next to a ring of two to four stages.
     P->nw = 16;
     P->spc = (nslab + sms - 1) / sms;
     P->G = (nslab + P->spc - 1) / P->spc;
-    const int U16 = 16 * slab_units_per_warp(Gm.bits, true, 16);
+    const int U16 = 16 * slab_units_per_warp(Gm.bits, 16);
     P->QPS = (Gm.KT + U16 - 1) / U16;
-    P->x_res = slab_ring(P, M, (U16 * Gm.unit_bytes + 127) / 128 * 128, xres, 4, kGemvSmemMax1 - 128) >= 2;
-    if (P->x_res) return TF_OK;
-    // (3) Eight warps, two CTAs per SM, x slices travelling with each stage.
-    P->nw = 8;
-    P->spc = (nslab + 2 * sms - 1) / (2 * sms);
-    P->G = (nslab + P->spc - 1) / P->spc;
-    const int Us = 8 * slab_units_per_warp(Gm.bits, false, 8);
-    P->QPS = (Gm.KT + Us - 1) / Us;
-    P->x_off = (Us * Gm.unit_bytes + 127) / 128 * 128;
-    if (slab_ring(P, M, P->x_off + Us * M * 256, 0, 16, kGemvSmemBudget) > 0) return TF_OK;
-    *P = GemvPlan{};  // stages too large for two CTAs per SM: the tile GEMV takes the layer
+    if (slab_ring(P, M, (U16 * Gm.unit_bytes + 127) / 128 * 128, xres, 4, kGemvSmemMax1 - 128) >= 2) return TF_OK;
+    // x does not fit even then: the tile GEMV takes the layer, reading each
+    // activation slice once per tile.  (Slices travelling with every slab
+    // stage, which each CTA re-reads from L2 for every slab, were slower:
+    // 232 against 212 us for 32768 x 32768 at M = 4.)
+    *P = GemvPlan{};
   }
   const int TPS = tiles_per_stage(Gm.bits);
   P->slab = false;
@@ -872,11 +846,9 @@ int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStre
 
 template <int BITS, int GPT>
 int launch_slab(const SlabArgs& a, int nw, int grid, size_t smem, cudaStream_t s) {
-  static std::atomic<unsigned long long> opted_res{0}, opted_res16{0}, opted_stage{0};
-  if (a.x_res && nw == 16)
-    return launch_pdl(gemv_slab_kernel<BITS, GPT, true, 16>, opted_res16, grid, 512, kGemvSmemMax1, smem, s, a);
-  if (a.x_res) return launch_pdl(gemv_slab_kernel<BITS, GPT, true, 8>, opted_res, grid, 256, kGemvSmemMax, smem, s, a);
-  return launch_pdl(gemv_slab_kernel<BITS, GPT, false, 8>, opted_stage, grid, 256, kGemvSmemMax, smem, s, a);
+  static std::atomic<unsigned long long> opted8{0}, opted16{0};
+  if (nw == 16) return launch_pdl(gemv_slab_kernel<BITS, GPT, 16>, opted16, grid, 512, kGemvSmemMax1, smem, s, a);
+  return launch_pdl(gemv_slab_kernel<BITS, GPT, 8>, opted8, grid, 256, kGemvSmemMax, smem, s, a);
 }
 
 // The GEMV of a checked layer with a plan; partials / counters are the
@@ -890,8 +862,8 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
     SlabArgs a;
     a.units = units; a.x = x; a.y = y; a.err = err;
     a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
-    a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS; a.x_res = P.x_res;
-    a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off; a.xres_off = P.xres_off;
+    a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS;
+    a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.xres_off = P.xres_off;
     a.red_off = P.red_off; a.ctl_off = P.ctl_off;
     if (G.bits == 4) {
       if (G.gpt == 1) return launch_slab<4, 1>(a, P.nw, P.G, P.smem, stream);

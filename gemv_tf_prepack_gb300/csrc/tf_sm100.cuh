@@ -135,12 +135,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-// Arrive on `bar` once every cp.async this thread has issued so far has
-// landed; the arrival is one of the barrier's expected arrivals (.noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // Shared-memory atomic add with acquire-release semantics at CTA scope: this
 // thread's earlier memory accesses (and those ordered before them) happen
 // before it, and its later ones after it.  Returns the old value.
