@@ -10,13 +10,15 @@
 // multiply-accumulate instead of CUDA-core FMAs.
 //
 // Two kernels share that inner step (one 16-row x 128-column unit per warp):
-//  * slab GEMV, for layers with at least as many 16-row slabs as SMs: each
-//    CTA owns whole slabs over all of K, its eight warps split K, and a
-//    slab's eight partial sums meet in shared memory.  No CTA waits on
-//    another, so a layer ends as soon as its last slab is done.
-//  * tile GEMV, for the rest (few rows or short K): K is split across CTAs
-//    too; a 128-row block shared by several CTAs is summed by the last of
-//    them, in a fixed order, from FP32 partials in a workspace.
+//  * slab GEMV, for layers with at least as many 16-row slabs as SMs whose
+//    activations fit in shared memory: each CTA owns whole slabs over all of
+//    K, its eight (or sixteen) warps split K, and a slab's partial sums meet
+//    in shared memory.  No CTA waits on another, so a layer ends as soon as
+//    its last slab is done.
+//  * tile GEMV, for the rest (few rows, short K, or activations too large to
+//    stay resident): K is split across CTAs too; a 128-row block shared by
+//    several CTAs is summed by the last of them, in a fixed order, from FP32
+//    partials in a workspace.
 #include <cuda_runtime.h>
 
 #include <atomic>

@@ -131,12 +131,16 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  * batch 1, and up to 8 rows at no extra cost): y[M, N] = x[M, K] * W^T.
  * Each weight code is read from HBM once, unpacked and dequantised to BF16 in
  * registers and fed straight to the tensor cores (mma.sync, FP32
- * accumulation).  The K dimension is split across all SMs so that the whole
- * chip streams weights; partial sums are combined by the last-arriving block
- * in a fixed order, so results are deterministic run to run.
+ * accumulation), with the whole chip streaming weights.  Layers with at
+ * least one 16-row slab per SM (and K >= 1024) give every block whole slabs
+ * and split K over the block's warps, with x resident in shared memory; the
+ * others (few rows, short K, or x too large to stay resident) split K across
+ * all blocks, and the last-arriving block of each row block adds the partial
+ * sums.  Every addition happens in a fixed order, so results are
+ * deterministic run to run.
  * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),
- * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size).
- * 1 <= M <= 8, else TF_ERR_UNSUPPORTED.
+ * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size; may
+ * be NULL when that is 0).  1 <= M <= 8, else TF_ERR_UNSUPPORTED.
  */
 int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
