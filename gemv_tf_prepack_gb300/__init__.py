@@ -21,7 +21,7 @@ import re
 import numpy as np
 
 __all__ = [
-    "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "unprepack",
+    "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "prepack_awq", "unprepack",
     "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemv_noalloc", "gemm",
     "gemm_workspace_size", "device_error",
     "header_declarations",
@@ -53,6 +53,7 @@ _SIGNATURES = {
     "tf_status_string": (ctypes.c_char_p, [_i]),
     "tf_prepack_size": (_i, [_i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tf_prepack": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _sz]),
+    "tf_prepack_awq": (_i, [_p, _p, _p, _i, _i, _i, _p, _sz]),
     "tf_unprepack": (_i, [_p, _sz, _p, _p, _p]),
     "tf_blob_info": (_i, [_p, _sz] + [ctypes.POINTER(_i)] * 4),
     "tf_dequant": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p]),
@@ -124,6 +125,29 @@ def prepack(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, N: int, 
     out = np.empty(prepack_size(N, K, bits, group), dtype=np.uint8)
     _check(_lib().tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, N, K, bits, group,
                              out.ctypes.data, out.size), "tf_prepack")
+    return out
+
+
+def prepack_awq(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, N: int, K: int,
+                group: int) -> np.ndarray:
+    """Pre-tiling of an INT4 layer in AWQ's checkpoint layout; returns the blob (uint8).
+
+    qweight int32 [K, N/8] and qzeros int32 [K/g, N/8] (eight output columns per word),
+    scales float16 (or their uint16 bits) [K/g, N]; the layout is described at
+    ``tf_prepack_awq`` in include/tf.h.
+    """
+    g = K if group == 0 else group
+    qw = np.ascontiguousarray(qweight).view(np.int32) if np.asarray(qweight).dtype.itemsize == 4 else None
+    qz = np.ascontiguousarray(qzeros).view(np.int32) if np.asarray(qzeros).dtype.itemsize == 4 else None
+    sc = np.ascontiguousarray(scales)
+    if qw is None or qz is None or sc.dtype.itemsize != 2:
+        raise ValueError("qweight/qzeros must be 32-bit and scales 16-bit arrays")
+    sc = sc.view(np.uint16)
+    if N % 8 or qw.shape != (K, N // 8) or qz.shape != (K // g, N // 8) or sc.shape != (K // g, N):
+        raise ValueError("qweight/qzeros/scales shapes do not match N, K, group")
+    out = np.empty(prepack_size(N, K, 4, group), dtype=np.uint8)
+    _check(_lib().tf_prepack_awq(qw.ctypes.data, qz.ctypes.data, sc.ctypes.data, N, K, group,
+                                 out.ctypes.data, out.size), "tf_prepack_awq")
     return out
 
 

@@ -1,7 +1,9 @@
 // Host side of libtf: the offline interleaved pre-tiling (TileFuse,
 // Methodology 2 "Interleaved pre-tiling": quantisation metadata packed into
 // the weight tiles, matrix reordered so that each consumer's tiles are
-// contiguous, valid up to 32K), its exact inverse, and the small status API.
+// contiguous, valid up to 32K), its exact inverse, the import of AWQ
+// checkpoints as published (Contributions 1: AWQ-style weights consumed
+// without re-quantising the model), and the small status API.
 #include <algorithm>
 #include <cstring>
 #include <thread>
@@ -14,7 +16,51 @@ using tf::Geometry;
 
 namespace {
 
-// Natural-order accessors with the padding rules of the blob format.
+// AWQ checkpoints keep INT4 layers in the layout of AWQ's GEMM kernels:
+// qweight int32 [K, N/8] and qzeros int32 [K/g, N/8] each hold the 4-bit
+// values of eight consecutive output columns 8c..8c+7 per word, nibble i
+// (bits 4i..4i+3) holding column 8c + kAwqOrder[i]; scales are FP16
+// [K/g, N].  kAwqNibble is the inverse map: the nibble of column 8c + j.
+constexpr int kAwqOrder[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+struct AwqNibbles {
+  int of[8];
+  constexpr AwqNibbles() : of() {
+    for (int i = 0; i < 8; ++i) of[kAwqOrder[i]] = i;
+  }
+};
+constexpr AwqNibbles kAwqNibble;
+
+inline int awq_nibble(uint32_t word, int j) { return (word >> (4 * kAwqNibble.of[j])) & 0xF; }
+
+// IEEE binary16 -> BF16, round to nearest even (every binary16 value is in
+// BF16's range; only the 10-bit fraction is rounded to 7 bits).
+uint16_t f16_to_bf16(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  const uint32_t e = (h >> 10) & 0x1Fu;
+  uint32_t m = h & 0x3FFu, f;  // f: the value as binary32 bits (exact)
+  if (e == 0x1Fu) {
+    f = sign | 0x7F800000u | (m << 13);
+  } else if (e != 0) {
+    f = sign | ((e + 112u) << 23) | (m << 13);  // exponent bias 15 -> 127
+  } else if (m == 0) {
+    f = sign;
+  } else {  // subnormal m * 2^-24: normalise the fraction
+    uint32_t ex = 113;
+    while (!(m & 0x400u)) { m <<= 1; --ex; }
+    f = sign | (ex << 23) | ((m & 0x3FFu) << 13);
+  }
+  if ((f & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((f >> 16) | 0x40u);  // NaN stays NaN
+  return (uint16_t)((f + 0x7FFFu + ((f >> 16) & 1u)) >> 16);
+}
+
+struct AwqArrays {
+  const uint32_t* qweight;  // [K, N/8]
+  const uint32_t* qzeros;   // [K/g, N/8]
+  const uint16_t* scales;   // FP16 bits [K/g, N]
+};
+
+// Natural-order accessors (or an AWQ checkpoint's, when awq is set) with the
+// padding rules of the blob format.
 struct Source {
   const Geometry& G;
   const uint8_t* q8;     // INT8 codes [N, K]
@@ -22,8 +68,10 @@ struct Source {
   const uint16_t* s;     // [N, K/g]
   const uint8_t* z;      // [N, K/g]
   int n_groups;
+  const AwqArrays* awq;
 
   int code(int n, int k) const {
+    if (awq) return awq_nibble(awq->qweight[(size_t)k * (G.N / 8) + n / 8], n & 7);
     if (G.bits == 4) return (q4[(size_t)n * (G.K / 8) + (k >> 3)] >> (4 * (k & 7))) & 0xF;
     return q8[(size_t)n * G.K + k];
   }
@@ -34,16 +82,22 @@ struct Source {
   int padded_code(int n, int k) const {
     if (n >= G.N) return 0;
     if (k < G.K) return code(n, k);
-    const int grp = group_of(k);
-    return grp < n_groups ? z[(size_t)n * n_groups + grp] : 0;
+    return zero(n, group_of(k));
   }
   uint16_t scale(int n, int grp) const {
-    return (n < G.N && grp < n_groups) ? s[(size_t)n * n_groups + grp] : 0;
+    if (n >= G.N || grp >= n_groups) return 0;
+    if (awq) return f16_to_bf16(awq->scales[(size_t)grp * G.N + n]);
+    return s[(size_t)n * n_groups + grp];
   }
   uint8_t zero(int n, int grp) const {
-    return (n < G.N && grp < n_groups) ? z[(size_t)n * n_groups + grp] : 0;
+    if (n >= G.N || grp >= n_groups) return 0;
+    if (awq) return (uint8_t)awq_nibble(awq->qzeros[(size_t)grp * (G.N / 8) + n / 8], n & 7);
+    return z[(size_t)n * n_groups + grp];
   }
 };
+
+// Header and units of the blob of G from src.
+void write_blob(const Geometry& G, const Source& src, uint8_t* o);
 
 // Unit row / column of code i of word j in slot p of K half h.
 inline void code_position(int h, int p, int j, int i, int* row, int* col) {
@@ -124,6 +178,17 @@ void parallel_slabs(int S, F&& f) {
   for (auto& t : th) t.join();
 }
 
+void write_blob(const Geometry& G, const Source& src, uint8_t* o) {
+  write_header(G, o);
+  parallel_slabs(G.S, [&](int s) {
+    for (int kt = 0; kt < G.KT; ++kt) {
+      uint8_t* unit = o + tf::unit_offset(G, s, kt);
+      std::memset(unit, 0, G.unit_bytes);
+      pack_unit(src, s, kt, unit);
+    }
+  });
+}
+
 }  // namespace
 
 extern "C" {
@@ -166,16 +231,22 @@ int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros
   const int qmax = (1 << bits) - 1;
   for (size_t i = 0; i < (size_t)N * n_groups; ++i)
     if (zeros[i] > qmax) return TF_ERR_INVALID_ARG;
-  Source src{G, (const uint8_t*)qweight, (const uint32_t*)qweight, scales, zeros, n_groups};
-  uint8_t* o = (uint8_t*)out;
-  write_header(G, o);
-  parallel_slabs(G.S, [&](int s) {
-    for (int kt = 0; kt < G.KT; ++kt) {
-      uint8_t* unit = o + tf::unit_offset(G, s, kt);
-      std::memset(unit, 0, G.unit_bytes);
-      pack_unit(src, s, kt, unit);
-    }
-  });
+  Source src{G, (const uint8_t*)qweight, (const uint32_t*)qweight, scales, zeros, n_groups, nullptr};
+  write_blob(G, src, (uint8_t*)out);
+  return TF_OK;
+}
+
+int tf_prepack_awq(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales_f16, int N,
+                   int K, int group, void* out, size_t out_bytes) {
+  if (!qweight || !qzeros || !scales_f16 || !out) return TF_ERR_INVALID_ARG;
+  if (N % 8 != 0) return TF_ERR_INVALID_ARG;
+  Geometry G;
+  int rc = tf::make_geometry(N, K, 4, group, &G);
+  if (rc) return rc;
+  if (out_bytes < G.total_bytes) return TF_ERR_INVALID_ARG;
+  const AwqArrays awq{(const uint32_t*)qweight, (const uint32_t*)qzeros, scales_f16};
+  Source src{G, nullptr, nullptr, nullptr, nullptr, K / G.g, &awq};
+  write_blob(G, src, (uint8_t*)out);
   return TF_OK;
 }
 

@@ -96,6 +96,27 @@ int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros
                int N, int K, int bits, int group, void* out, size_t out_bytes);
 
 /*
+ * Offline pre-tiling of an INT4 layer as AWQ checkpoints store it (TileFuse,
+ * Contributions 1: the fused kernels take AWQ-style weights as published,
+ * with no re-quantisation of the model); host, synchronous, pure.
+ * Input layout (AWQ's GEMM format):
+ *   qweight     int32 [K, N/8]: word (k, c) holds the codes of W[8c + j, k],
+ *               j = 0..7, with the code of column 8c + j in nibble
+ *               (0, 4, 1, 5, 2, 6, 3, 7)[j] (bits 4*nibble .. 4*nibble+3);
+ *               equivalently nibble i holds column 8c + (0, 2, 4, 6, 1, 3, 5, 7)[i];
+ *   qzeros      int32 [K/g, N/8]: the zero points, packed the same way;
+ *   scales_f16  IEEE binary16 bits [K/g, N].
+ * g = group, or K for group = 0 (one group per row); group as for tf_prepack.
+ * Each scale is rounded to BF16 (round to nearest even), since the blob and
+ * the kernels dequantise to BF16 as bf16_rne((q - z) * s); the result is the
+ * blob tf_prepack makes from the same codes, zeros and those BF16 scales.
+ * N must be a multiple of 8 (TF_ERR_INVALID_ARG otherwise); out is a host
+ * buffer of at least tf_prepack_size(N, K, 4, group) bytes.
+ */
+int tf_prepack_awq(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales_f16,
+                   int N, int K, int group, void* out, size_t out_bytes);
+
+/*
  * Exact inverse of tf_prepack (host).  Reads N, K, bits, group from the
  * header and writes natural-order qweight, scales and zeros (sizes as for
  * tf_prepack).  TF_ERR_BAD_BLOB if the header is inconsistent with bytes.

@@ -237,3 +237,22 @@ def test_random_layers(N, K, bits, group, M):
     if M <= 8:
         check_close(to_host_bits(tf.gemv(W, x)), ref, f"gemv {N}x{K} w{bits} g{group} M={M}")
     assert tf.device_error() == 0
+
+
+# AWQ checkpoints imported with tf_prepack_awq: the device dequantises exactly
+# what the oracle decodes from the AWQ arrays, and both kernels match it.
+@pytest.mark.parametrize("N,K,group", [(1032, 1024, 128), (4096, 4096, 128), (2440, 1536, 64), (512, 768, 0)])
+def test_awq_import_parity(N, K, group):
+    from oracle import awq
+    qw = synth.make_weights(N, K, 4, group, 31)
+    q = tf_oracle.unpack(qw.qweight, 4, K)
+    s16 = (np.random.default_rng([31, 7]).random(qw.scales.shape) * 0.01 + 0.001).astype(np.float16)
+    qweight, qzeros, scales = awq.awq_encode(q, qw.zeros, s16)
+    W = tf.Weights.upload(tf.prepack_awq(qweight, qzeros, scales, N, K, group))
+    qd, sd, zd = awq.awq_decode(qweight, qzeros, scales, N, K, group)
+    np.testing.assert_array_equal(to_host_bits(tf.dequant(W)), tf_oracle.dequant_bits(qd, sd, zd, group))
+    wd = tf_oracle.dequant(qd, sd, zd, group)
+    for M, fn in ((1, tf.gemv), (8, tf.gemv), (64, tf.gemm)):
+        xb = synth.make_activations(M, K, 31)
+        y = to_host_bits(fn(W, to_dev_bf16(xb)))
+        check_close(y, tf_oracle.linear_f64(xb, wd), f"awq {fn.__name__} {N}x{K} g{group} M={M}")
