@@ -59,8 +59,10 @@ _SIGNATURES = {
     "tf_dequant": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p]),
     "tf_gemv_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tf_gemv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
+    "tf_gemv_bias": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
     "tf_gemm_workspace_size": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
+    "tf_gemm_bias": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
     "tf_gemv_noalloc": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
     "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
 }
@@ -278,14 +280,25 @@ def dequant(W: Weights, out=None, stream=None):
     return out
 
 
-def gemv(W: Weights, x, y=None, workspace=None, stream=None):
-    """y[M, N] = x[M, K] W^T for 1 <= M <= 8 (fused unpack + dequant + mma.sync, split-K)."""
+def _check_bias(W: Weights, bias):
+    torch = _torch()
+    if bias.dtype != torch.bfloat16 or tuple(bias.shape) != (W.N,) or not bias.is_cuda or not bias.is_contiguous():
+        raise ValueError(f"bias must be a contiguous CUDA bfloat16 tensor [{W.N}]")
+
+
+def gemv(W: Weights, x, y=None, workspace=None, stream=None, bias=None):
+    """y[M, N] = x[M, K] W^T (+ bias[N]) for 1 <= M <= 8 (fused unpack + dequant + mma.sync)."""
     _check_x(W, x)
     M = x.shape[0]
     y = _out(W, M, y)
     wp, wn = _workspace_args(W, M, "gemv", workspace)
-    _check(_lib().tf_gemv(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(), M,
-                          wp, wn, _stream_handle(stream)), "tf_gemv")
+    if bias is None:
+        _check(_lib().tf_gemv(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(),
+                              M, wp, wn, _stream_handle(stream)), "tf_gemv")
+    else:
+        _check_bias(W, bias)
+        _check(_lib().tf_gemv_bias(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(),
+                                   bias.data_ptr(), y.data_ptr(), M, wp, wn, _stream_handle(stream)), "tf_gemv_bias")
     return y
 
 
@@ -309,8 +322,8 @@ def gemm_workspace_size(N: int, K: int, bits: int, group: int, M: int) -> int:
     return out.value
 
 
-def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True):
-    """y[M, N] = x[M, K] W^T for any M (fused dequant to SMEM + tcgen05 MMAs).
+def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True, bias=None):
+    """y[M, N] = x[M, K] W^T (+ bias[N]) for any M (fused dequant to SMEM + tcgen05 MMAs).
 
     With stream_k (default) the layer's cached workspace lets the last,
     partial wave of output tiles be split along K across all SMs; with
@@ -323,8 +336,13 @@ def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True):
         wp, wn = _workspace_args(W, M, "gemm", workspace)
     else:
         wp, wn = None, 0
-    _check(_lib().tf_gemm(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(), M,
-                          wp, wn, _stream_handle(stream)), "tf_gemm")
+    if bias is None:
+        _check(_lib().tf_gemm(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(), y.data_ptr(),
+                              M, wp, wn, _stream_handle(stream)), "tf_gemm")
+    else:
+        _check_bias(W, bias)
+        _check(_lib().tf_gemm_bias(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(),
+                                   bias.data_ptr(), y.data_ptr(), M, wp, wn, _stream_handle(stream)), "tf_gemm_bias")
     return y
 
 

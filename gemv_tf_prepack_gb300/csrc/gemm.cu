@@ -62,6 +62,7 @@ enum : unsigned {
 struct GemmArgs {
   const uint8_t* units;
   uint16_t* y;
+  const uint16_t* bias;       // BF16 [N] added before the final rounding, or null
   unsigned* err;              // device error word
   float* ws;                  // stream-K partial sums: [CTA][2][BN / 16][128 rows][16]
   unsigned* cnt;              // stream-K arrivals per tile (zero on entry and on exit)
@@ -311,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (!ok) break;
       tc_fence_after();
       const int n = nb * kTileN + row;
+      const bool has_bias = a.bias != nullptr;
+      const float bv = has_bias && n < a.N ? bf16_bits_to_float(a.bias[n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256;
       const bool whole = wk.kb == 0 && wk.ke == a.KT;
       const int ti = wk.tile - a.dp_tiles;
@@ -332,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint16_t* stg = reinterpret_cast<uint16_t*>(smem + a.off_epi) + buf * (kEpiChunk * kTileN);
 #pragma unroll
             for (int j = 0; j < kEpiChunk; ++j)
-              stg[j * kTileN + row] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+              stg[j * kTileN + row] = __bfloat16_as_ushort(
+                  __float2bfloat16_rn(has_bias ? __uint_as_float(r[j]) + bv : __uint_as_float(r[j])));
             fence_async_shared();
             named_barrier_sync(kEpilogueThreads);
             if (row == 0) {
@@ -347,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int j = 0; j < 16; ++j) {
               const int m = m0 + j;
               if (m < a.M)
-                a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+                a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(has_bias ? __uint_as_float(r[j]) + bv : __uint_as_float(r[j])));
             }
           }
         } else {
@@ -405,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 if (m0 + 4 * j + e < a.M)
-                  a.y[(size_t)(m0 + 4 * j + e) * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(vv[e]));
+                  a.y[(size_t)(m0 + 4 * j + e) * a.N + n] =
+                      __bfloat16_as_ushort(__float2bfloat16_rn(has_bias ? vv[e] + bv : vv[e]));
             }
           }
         }
@@ -640,6 +646,12 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
 
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x, uint16_t* y,
             int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return tf_gemm_bias(blob, blob_bytes, N, K, bits, group, x, nullptr, y, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                 const uint16_t* bias, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
   Geometry G;
   int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
   if (rc) return rc;
@@ -653,6 +665,7 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
   P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   P.a.y = y;
+  P.a.bias = bias;
   P.a.err = device_error_ptr();
   if (!P.a.err) return TF_ERR_CUDA;
   CUtensorMap map, wmap, ymap;

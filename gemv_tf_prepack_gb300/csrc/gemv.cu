@@ -189,16 +189,20 @@ __device__ __forceinline__ void mma_unit(const WRegs<BITS, GPT>& R, const uint32
   mma_half(R, 1, xs[1], acc[1]);
 }
 
-// v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1.
-__device__ __forceinline__ void store_y(uint16_t* y, int N, int M, int n0, int t, const float (&v)[4]) {
+// v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1; bias
+// (BF16 [N], or null) is added to each sum before its one rounding to BF16.
+__device__ __forceinline__ void store_y(uint16_t* y, const uint16_t* bias, int N, int M, int n0, int t,
+                                        const float (&v)[4]) {
   const int m0 = 2 * t, m1 = 2 * t + 1, n1 = n0 + 8;
   if (n0 < N) {
-    if (m0 < M) y[(size_t)m0 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
-    if (m1 < M) y[(size_t)m1 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
+    const float b = bias ? bf16_bits_to_float(bias[n0]) : 0.f;
+    if (m0 < M) y[(size_t)m0 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[0] + b : v[0]));
+    if (m1 < M) y[(size_t)m1 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[1] + b : v[1]));
   }
   if (n1 < N) {
-    if (m0 < M) y[(size_t)m0 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2]));
-    if (m1 < M) y[(size_t)m1 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[3]));
+    const float b = bias ? bf16_bits_to_float(bias[n1]) : 0.f;
+    if (m0 < M) y[(size_t)m0 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[2] + b : v[2]));
+    if (m1 < M) y[(size_t)m1 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[3] + b : v[3]));
   }
 }
 
@@ -241,6 +245,7 @@ static_assert(tiles_per_stage(4) * kSlabsPerTile <= 32 && tiles_per_stage(8) * k
 struct GemvArgs {
   const uint8_t* units;
   uint16_t* y;
+  const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
   float4* partials;    // [G][S_max][8 warps][32 lanes]
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
   unsigned* err;
@@ -266,7 +271,7 @@ __device__ __forceinline__ bool end_segment(const GemvArgs& a, int c, long long 
                                             int lane, const float (&v)[4]) {
   const int gr = lane >> 2, t = lane & 3;
   if (whole) {
-    store_y(a.y, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, v);
+    store_y(a.y, a.bias, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, v);
     return false;
   }
   const int seg = nb - (int)(t0 / a.KT);
@@ -306,7 +311,7 @@ __device__ __forceinline__ void publish_segment(const GemvArgs& a, int nb, int w
       }
     }
   }
-  store_y(a.y, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, s);
+  store_y(a.y, a.bias, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, s);
   if (lane == 0) a.counters[nb * 8 + warp] = 0u;
 }
 
@@ -505,6 +510,7 @@ struct SlabArgs {
   const uint8_t* units;
   const uint16_t* x;
   uint16_t* y;
+  const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
   unsigned* err;
   int N, K, M, KT, g;
   int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
@@ -700,7 +706,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
           v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
         }
       }
-      store_y(a.y, a.N, a.M, (s0 + i) * kSlabN + gr, t, v);
+      store_y(a.y, a.bias, a.N, a.M, (s0 + i) * kSlabN + gr, t, v);
     }
   }
   if (threadIdx.x == 0 && ctl[1]) {
@@ -855,14 +861,14 @@ int launch_slab(const SlabArgs& a, int nw, int grid, size_t smem, cudaStream_t s
 
 // The GEMV of a checked layer with a plan; partials / counters are the
 // tile GEMV's scratch (unused by the slab GEMV).
-int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint16_t* x, uint16_t* y, int M,
-             float4* partials, unsigned* counters, cudaStream_t stream) {
+int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
+             uint16_t* y, int M, float4* partials, unsigned* counters, cudaStream_t stream) {
   unsigned* err = device_error_ptr();
   if (!err) return TF_ERR_CUDA;
   const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   if (P.slab) {
     SlabArgs a;
-    a.units = units; a.x = x; a.y = y; a.err = err;
+    a.units = units; a.x = x; a.y = y; a.bias = bias; a.err = err;
     a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
     a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS;
     a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.xres_off = P.xres_off;
@@ -880,7 +886,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
   int rc = encode_x_map(x, M, G.K, &map);
   if (rc) return rc;
   GemvArgs a;
-  a.units = units; a.y = y; a.partials = partials; a.counters = counters; a.err = err;
+  a.units = units; a.y = y; a.bias = bias; a.partials = partials; a.counters = counters; a.err = err;
   a.T = P.T;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
   a.G = P.G; a.S_max = P.S_max;
@@ -943,6 +949,12 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
 
 int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
             uint16_t* y, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return tf_gemv_bias(blob, blob_bytes, N, K, bits, group, x, nullptr, y, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                 const uint16_t* bias, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
   Geometry G;
   int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
   if (rc) return rc;
@@ -954,7 +966,7 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
   if (rc) return rc;
   const size_t need = gemv_scratch_bytes(P);
   if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
-  return run_gemv(G, P, blob, x, y, M, static_cast<float4*>(workspace),
+  return run_gemv(G, P, blob, x, bias, y, M, static_cast<float4*>(workspace),
                   need ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes) : nullptr,
                   stream);
 }
@@ -1008,15 +1020,15 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
   if (gemv_scratch_bytes(P) > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
-  if (P.slab) return run_gemv(G, P, blob, x, y, M, nullptr, nullptr, stream);
+  if (P.slab) return run_gemv(G, P, blob, x, nullptr, y, M, nullptr, nullptr, stream);
   unsigned char* scratch = gemv_scratch_address();
   if (!scratch) return TF_ERR_CUDA;
   // The arrival counters must start at zero; a call cut short (device error)
   // could have left them dirty, so clear them on the stream first.
   unsigned char* counters = scratch + P.partial_bytes;
   if (cudaMemsetAsync(counters, 0, P.counter_bytes, stream) != cudaSuccess) return TF_ERR_CUDA;
-  return run_gemv(G, P, blob, x, y, M, reinterpret_cast<float4*>(scratch), reinterpret_cast<unsigned*>(counters),
-                  stream);
+  return run_gemv(G, P, blob, x, nullptr, y, M, reinterpret_cast<float4*>(scratch),
+                  reinterpret_cast<unsigned*>(counters), stream);
 }
 
 }  // extern "C"

@@ -11,6 +11,9 @@
 
 namespace tf {
 
+// A BF16 bit pattern as the float it denotes (exact: BF16 is the top half of binary32).
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
 // ---------------------------------------------------------------------------
 // packed BF16x2 arithmetic (native on sm_90 and later; round to nearest even)
 

@@ -168,6 +168,17 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
             cudaStream_t stream);
 
 /*
+ * tf_gemv with a bias in the epilogue: y[m, n] = bf16_rne(sum_k x[m, k] *
+ * w[n, k] + bias[n]), the BF16 bias added to the FP32 sum before its one
+ * rounding (a fused epilogue; the pages' kernels end at the product).  bias
+ * is a device array of N BF16 values (2-byte aligned), or NULL for none
+ * (exactly tf_gemv).  Everything else as for tf_gemv.
+ */
+int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                 const uint16_t* x, const uint16_t* bias, uint16_t* y, int M, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Workspace bytes tf_gemm needs on the current device for this layer and M
  * to split the K dimension of its last, partial wave of output tiles across
  * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters.  0
@@ -190,6 +201,15 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
             cudaStream_t stream);
+
+/*
+ * tf_gemm with a bias in the epilogue: y[m, n] = bf16_rne(sum_k x[m, k] *
+ * w[n, k] + bias[n]) (bias: device, N BF16 values, 2-byte aligned, or NULL
+ * for none, which is exactly tf_gemm).  Everything else as for tf_gemm.
+ */
+int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                 const uint16_t* x, const uint16_t* bias, uint16_t* y, int M, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * tf_gemv without a caller-provided workspace, for callers that cannot

@@ -256,3 +256,35 @@ def test_awq_import_parity(N, K, group):
         xb = synth.make_activations(M, K, 31)
         y = to_host_bits(fn(W, to_dev_bf16(xb)))
         check_close(y, tf_oracle.linear_f64(xb, wd), f"awq {fn.__name__} {N}x{K} g{group} M={M}")
+
+
+# Bias in the epilogue (tf_gemv_bias / tf_gemm_bias): y = bf16_rne(x W^T + bias).
+# The shapes reach every place y is written: slab GEMV, tile GEMV (whole row
+# blocks and the split-K last arriver), GEMM TMA-staged whole tiles, GEMM
+# element stores (N % 8 != 0) and the GEMM stream-K fixup.
+BIAS_CASES = [
+    (2440, 1152, 4, 128, 1, "gemv"), (2440, 1152, 8, 0, 3, "gemv"), (200, 192, 4, 64, 8, "gemv"),
+    (1000, 1016, 4, 0, 1, "gemv"), (384, 4096, 8, 64, 37, "gemm"), (20000, 1016, 4, 0, 40, "gemm"),
+    (2048, 1536, 4, 128, 512, "gemm"), (1004, 1016, 4, 0, 300, "gemm"),
+]
+
+
+@pytest.mark.parametrize("N,K,bits,group,M,fn", BIAS_CASES)
+def test_bias_epilogue(N, K, bits, group, M, fn):
+    import torch
+    qw, W = layer(N, K, bits, group, 47)
+    xb = synth.make_activations(M, K, 47, outliers=fn == "gemm")
+    b16 = (np.random.default_rng([47, N]).standard_normal(N) * 0.5).astype(np.float32)
+    bias_bits = tf_oracle.bf16_value_to_bits(tf_oracle.bf16_round(b16.astype(np.float64)))
+    bias = to_dev_bf16(bias_bits)
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb) \
+        + tf_oracle.bf16_bits_to_f64(bias_bits)[None, :]
+    call = tf.gemv if fn == "gemv" else tf.gemm
+    y = to_host_bits(call(W, to_dev_bf16(xb), bias=bias))
+    check_close(y, ref, f"{fn}+bias {N}x{K} w{bits} g{group} M={M}")
+    if fn == "gemm":  # every tile whole (no workspace): the other schedule's epilogue
+        y2 = to_host_bits(tf.gemm(W, to_dev_bf16(xb), bias=bias, stream_k=False))
+        check_close(y2, ref, f"gemm+bias whole tiles {N}x{K} M={M}")
+    with pytest.raises(ValueError):
+        call(W, to_dev_bf16(xb), bias=bias[:-1])
+    torch.cuda.synchronize()
