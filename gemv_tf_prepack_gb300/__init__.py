@@ -139,12 +139,12 @@ def prepack_awq(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, N: 
     ``tf_prepack_awq`` in include/tf.h.
     """
     g = K if group == 0 else group
-    qw = np.ascontiguousarray(qweight).view(np.int32) if np.asarray(qweight).dtype.itemsize == 4 else None
-    qz = np.ascontiguousarray(qzeros).view(np.int32) if np.asarray(qzeros).dtype.itemsize == 4 else None
-    sc = np.ascontiguousarray(scales)
-    if qw is None or qz is None or sc.dtype.itemsize != 2:
-        raise ValueError("qweight/qzeros must be 32-bit and scales 16-bit arrays")
-    sc = sc.view(np.uint16)
+    qw, qz, sc = np.ascontiguousarray(qweight), np.ascontiguousarray(qzeros), np.ascontiguousarray(scales)
+    if qw.dtype not in (np.int32, np.uint32) or qz.dtype not in (np.int32, np.uint32):
+        raise ValueError("qweight and qzeros must be int32 (or uint32) arrays of packed nibbles")
+    if sc.dtype not in (np.float16, np.uint16, np.int16):
+        raise ValueError("scales must be float16 (or their 16-bit patterns)")
+    qw, qz, sc = qw.view(np.int32), qz.view(np.int32), sc.view(np.uint16)
     if N % 8 or qw.shape != (K, N // 8) or qz.shape != (K // g, N // 8) or sc.shape != (K // g, N):
         raise ValueError("qweight/qzeros/scales shapes do not match N, K, group")
     out = np.empty(prepack_size(N, K, 4, group), dtype=np.uint8)

@@ -656,7 +656,8 @@ int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
   int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
   if (rc) return rc;
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace)) return TF_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(bias) & 1))
+    return TF_ERR_ALIGNMENT;
   GemmPlan P;
   rc = gemm_plan(G, M, workspace != nullptr, &P);
   if (rc) return rc;

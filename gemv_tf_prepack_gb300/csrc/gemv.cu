@@ -960,7 +960,7 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
   if (rc) return rc;
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
   if (M > 8) return TF_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(workspace)) return TF_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(bias) & 1)) return TF_ERR_ALIGNMENT;
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;

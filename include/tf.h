@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define TF_VERSION 2
+#define TF_VERSION 3  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias */
 
 #define TF_OK 0
 #define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */
@@ -171,8 +171,8 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
  * tf_gemv with a bias in the epilogue: y[m, n] = bf16_rne(sum_k x[m, k] *
  * w[n, k] + bias[n]), the BF16 bias added to the FP32 sum before its one
  * rounding (a fused epilogue; the pages' kernels end at the product).  bias
- * is a device array of N BF16 values (2-byte aligned), or NULL for none
- * (exactly tf_gemv).  Everything else as for tf_gemv.
+ * is a device array of N BF16 values, or NULL for none (exactly tf_gemv);
+ * an odd address gives TF_ERR_ALIGNMENT.  Everything else as for tf_gemv.
  */
 int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
                  const uint16_t* x, const uint16_t* bias, uint16_t* y, int M, void* workspace,
@@ -204,8 +204,9 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
 
 /*
  * tf_gemm with a bias in the epilogue: y[m, n] = bf16_rne(sum_k x[m, k] *
- * w[n, k] + bias[n]) (bias: device, N BF16 values, 2-byte aligned, or NULL
- * for none, which is exactly tf_gemm).  Everything else as for tf_gemm.
+ * w[n, k] + bias[n]) (bias: device, N BF16 values, or NULL for none, which
+ * is exactly tf_gemm; an odd address gives TF_ERR_ALIGNMENT).  Everything
+ * else as for tf_gemm.
  */
 int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
                  const uint16_t* x, const uint16_t* bias, uint16_t* y, int M, void* workspace,

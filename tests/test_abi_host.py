@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol():
     lib = tf.lib()
     for d in decl:
         getattr(lib, d)
-    assert tf.version() == 2
+    assert tf.version() == 3
 
 
 @pytest.mark.parametrize("N,K,bits,group", [
@@ -126,5 +126,12 @@ def test_device_calls_validate_before_touching_the_gpu():
     assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 0, None, 0, None) == -1
     assert lib.tf_gemm(blob, size, 256, 512, 4, 128, ctypes.c_void_p(8194), y, 4, None, 0, None) == -3
     assert lib.tf_gemm(blob, size, 256, 512, 4, 128, x, y, 4, ctypes.c_void_p(8200), 64, None) == -3
+    # the bias variants: an odd bias address, and the same checks as the plain calls
+    odd = ctypes.c_void_p(20001)
+    assert lib.tf_gemv_bias(blob, size, 256, 512, 4, 128, x, odd, y, 1, None, 0, None) == -3
+    assert lib.tf_gemm_bias(blob, size, 256, 512, 4, 128, x, odd, y, 4, None, 0, None) == -3
+    assert lib.tf_gemv_bias(blob, size, 256, 512, 4, 128, x, None, y, 9, None, 0, None) == -2
+    assert lib.tf_gemv_bias(blob, size - 16, 256, 512, 4, 128, x, None, y, 1, None, 0, None) == -5
+    assert lib.tf_gemm_bias(blob, size, 256, 512, 4, 128, x, None, None, 4, None, 0, None) == -1
     assert lib.tf_dequant(None, size, 256, 512, 4, 128, y, None) == -1
     assert lib.tf_dequant(blob, size, 256, 512, 4, 96, y, None) == -2

@@ -157,3 +157,7 @@ def test_awq_errors():
     assert L.tf_prepack_awq(P(qw), P(qz), P(s16), 16, 128, 128, P(out), out.size) == 0
     with pytest.raises(ValueError):
         tf.prepack_awq(qw, qz, s16, 12, 128, 128)
+    with pytest.raises(ValueError):  # float data is not reinterpreted as packed nibbles
+        tf.prepack_awq(qw.astype(np.float32), qz, s16, 16, 128, 128)
+    with pytest.raises(ValueError):
+        tf.prepack_awq(qw, qz, s16.astype(np.float32), 16, 128, 128)
