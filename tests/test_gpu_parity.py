@@ -288,3 +288,18 @@ def test_bias_epilogue(N, K, bits, group, M, fn):
     with pytest.raises(ValueError):
         call(W, to_dev_bf16(xb), bias=bias[:-1])
     torch.cuda.synchronize()
+
+
+# Symmetric quantisation (no zero-point tensor in the checkpoint) is the
+# constant zero point 2^(bits-1): w = (q - 8) * s for INT4, (q - 128) * s for INT8.
+@pytest.mark.parametrize("N,K,bits,group", [(2440, 1024, 4, 128), (512, 768, 8, 64), (300, 256, 4, 32)])
+def test_symmetric_zero_point(N, K, bits, group):
+    qw = synth.make_weights(N, K, bits, group, 53)
+    zeros = np.full_like(qw.zeros, 1 << (bits - 1))
+    W = tf.Weights.upload(tf.prepack(qw.qweight, qw.scales, zeros, N, K, bits, group))
+    q = tf_oracle.unpack(qw.qweight, bits, K)
+    np.testing.assert_array_equal(to_host_bits(tf.dequant(W)), tf_oracle.dequant_bits(q, qw.scales, zeros, group))
+    for M, fn in ((1, tf.gemv), (24, tf.gemm)):
+        xb = synth.make_activations(M, K, 53)
+        ref = tf_oracle.reference(qw.qweight, qw.scales, zeros, bits, group, K, xb)
+        check_close(to_host_bits(fn(W, to_dev_bf16(xb))), ref, f"symmetric {fn.__name__} {N}x{K} w{bits} M={M}")
