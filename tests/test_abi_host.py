@@ -135,3 +135,34 @@ def test_device_calls_validate_before_touching_the_gpu():
     assert lib.tf_gemm_bias(blob, size, 256, 512, 4, 128, x, None, None, 4, None, 0, None) == -1
     assert lib.tf_dequant(None, size, 256, 512, 4, 128, y, None) == -1
     assert lib.tf_dequant(blob, size, 256, 512, 4, 96, y, None) == -2
+
+
+def test_header_serves_a_plain_c_client(tmp_path):
+    """include/tf.h compiles as C11 and a C program links against libtf and calls it."""
+    import os
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = next((d for d in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda")
+                     if d and os.path.exists(os.path.join(d, "include", "cuda_runtime_api.h"))), None)
+    if cuda_inc is None:
+        pytest.skip("cuda_runtime_api.h not found")
+    pkg = os.path.dirname(tf.lib_path)
+    src = tmp_path / "client.c"
+    src.write_text(
+        '#include "tf.h"\n#include <stdio.h>\n'
+        "int main(void) {\n"
+        "  size_t bytes = 0;\n"
+        "  int rc = tf_prepack_size(4096, 4096, 4, 128, &bytes);\n"
+        "  size_t unused = 0;\n"
+        "  int bad = tf_prepack_size(4096, 4096, 3, 128, &unused);  /* 3-bit codes: unsupported */\n"
+        '  printf("%d %d %zu %d %s\\n", tf_version(), rc, bytes, bad, tf_status_string(bad));\n'
+        "  return rc;\n}\n")
+    exe = tmp_path / "client"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.dirname(tf.HEADER), "-I",
+                    os.path.join(cuda_inc, "include"), str(src), "-o", str(exe), "-L", pkg, "-ltf",
+                    "-Wl,-rpath," + pkg], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out[:4] == [str(tf.version()), "0", str(tf.prepack_size(4096, 4096, 4, 128)), "-2"]
+    assert out[4] == "TF_ERR_UNSUPPORTED:"
