@@ -17,8 +17,8 @@
  * Conventions shared by every call:
  *  - bits is 4 or 8.  group is 32, 64, any multiple of 128 that divides K,
  *    or 0 for per output channel (one group spanning all of K).  K must be
- *    a multiple of 8 and of the group.  1 <= N, K <= 32768 (the pages'
- *    "dimensions up to 32K", Contributions 2).
+ *    a multiple of 8 and of the group.  1 <= N, K <= 32768 (Contributions 2:
+ *    the layout stays valid for dimensions up to 32K).
  *  - BF16 values are passed as their uint16 bit patterns.
  *  - Natural-order inputs (host memory): INT4 qweight is uint32 [N, K/8],
  *    eight codes per word, low nibble first along K; INT8 qweight is uint8
