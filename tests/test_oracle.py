@@ -210,9 +210,28 @@ def pin_brute_force_rational(O):
                 assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (bits, g, K, m, n, y[m, n], ref)
 
 
+def pin_single_nonzero_group(O):
+    """W whose only nonzero group is group j of row n: y[:, n] is that group's 128-term dot
+    product (exact Fractions), every other output is 0.  A wrong group-to-column map fails."""
+    rng = np.random.default_rng(17)
+    N, K, g, M = 4, 512, 128, 2
+    for n0, j in [(1, 2), (3, 0), (0, 3)]:
+        q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+        s = np.zeros((N, K // g), np.uint16)          # scale 0: the group dequantises to 0
+        z = rng.integers(0, 16, size=(N, K // g)).astype(np.uint8)
+        s[n0, j] = 0x3F00                              # 0.5
+        x = synth.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+        y = O.reference(synth.pack_w4(q), s, z, 4, g, K, x)
+        for m in range(M):
+            want = sum(bits_to_frac(int(x[m, k])) * (int(q[n0, k]) - int(z[n0, j])) * Fraction(1, 2)
+                       for k in range(j * g, (j + 1) * g))
+            assert abs(y[m, n0] - float(want)) <= 1e-12 * max(1.0, abs(float(want)))
+            assert all(y[m, n] == 0.0 for n in range(N) if n != n0)
+
+
 PINS = [pin_bf16_vs_torch, pin_bf16_hand_ties, pin_unpack_single_nibble,
         pin_dequant_power_of_two_scale, pin_dequant_all_pairs_rational, pin_dequant_groups,
-        pin_golden_worked_example, pin_closed_forms, pin_brute_force_rational]
+        pin_golden_worked_example, pin_closed_forms, pin_brute_force_rational, pin_single_nonzero_group]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
