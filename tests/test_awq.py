@@ -115,7 +115,7 @@ def test_c_f16_to_bf16_exhaustive():
 
 
 @pytest.mark.parametrize("N,K,group", [(264, 512, 128), (48, 384, 64), (8, 96, 32), (136, 200, 0),
-                                       (1032, 1024, 128), (72, 640, 128)])
+                                       (1032, 1024, 128), (72, 640, 128), (64, 1024, 256), (40, 768, 384)])
 def test_awq_blob_equals_natural_blob(N, K, group):
     (qweight, qzeros, s16), _ = _awq_layer(N, K, group, 11)
     blob = tf.prepack_awq(qweight, qzeros, s16, N, K, group)
