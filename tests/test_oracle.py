@@ -229,9 +229,47 @@ def pin_single_nonzero_group(O):
             assert all(y[m, n] == 0.0 for n in range(N) if n != n0)
 
 
+def _row_constant_layer(N, K):
+    """A W4 layer whose row n is the constant code q_n with zero z_n and a power-of-two
+    scale s_n, all three varying with n: with all-ones x, y[n] = K (q_n - z_n) s_n
+    exactly, so every output names the row it came from."""
+    n = np.arange(N)
+    q = (n % 16).astype(np.uint8)
+    z = ((n // 16) % 13).astype(np.uint8)                 # periods 208 and 1792 rows: no two
+    e = (n // 256) % 7                                     # 2048-row chunks look alike; s_n = 2^(e_n - 4)
+    s = (0x3F80 + ((e.astype(np.int64) - 4) << 7)).astype(np.uint16)
+    qweight = synth.pack_w4(np.repeat(q[:, None], K, axis=1))
+    want = K * (q.astype(np.float64) - z) * np.ldexp(1.0, (e - 4).astype(np.int64))
+    return qweight, s[:, None], z[:, None], want
+
+
+def pin_rows_and_chunks(O):
+    """reference() past its 2048-row chunks, and reference_rows() for unsorted, repeated rows
+    spread over those chunks: both against the closed form K (q_n - z_n) s_n, and
+    reference_rows() on one-hot x against the requested columns of q."""
+    N, K = 4200, 64
+    qweight, s, z, want = _row_constant_layer(N, K)
+    ones = np.full((2, K), 0x3F80, np.uint16)
+    y = O.reference(qweight, s, z, 4, 0, K, ones)
+    np.testing.assert_array_equal(y, np.broadcast_to(want, (2, N)))
+    rows = np.array([4199, 3, 2048, 2047, 3, 4096, 100, 4095, 2049, 0])
+    yr = O.reference_rows(qweight, s, z, 4, 0, K, ones, rows)
+    np.testing.assert_array_equal(yr, np.broadcast_to(want[rows], (2, rows.size)))
+    # one-hot x, z = 0, s = 1: output i is q[rows[i], k]
+    rng = np.random.default_rng(29)
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    for k in (0, 37):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        yr = O.reference_rows(synth.pack_w4(q), np.full((N, 1), 0x3F80, np.uint16), np.zeros((N, 1), np.uint8),
+                              4, 0, K, x, rows)
+        np.testing.assert_array_equal(yr[0], q[rows, k].astype(np.float64))
+
+
 PINS = [pin_bf16_vs_torch, pin_bf16_hand_ties, pin_unpack_single_nibble,
         pin_dequant_power_of_two_scale, pin_dequant_all_pairs_rational, pin_dequant_groups,
-        pin_golden_worked_example, pin_closed_forms, pin_brute_force_rational, pin_single_nonzero_group]
+        pin_golden_worked_example, pin_closed_forms, pin_brute_force_rational, pin_single_nonzero_group,
+        pin_rows_and_chunks]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -318,7 +356,35 @@ def _bad_linear_float32(x_bits, wd, rows_per_chunk=4096):
     return (x @ np.asarray(wd, np.float32).T).astype(np.float64)
 
 
+def _bad_rows_metadata_by_position(qweight, scales_bits, zeros, bits, group, K, x_bits, rows):
+    """Codes taken for the requested rows, scales and zeros by position instead."""
+    rows = np.asarray(rows)
+    q = tf_oracle.unpack(qweight[rows], bits, K)
+    wd = tf_oracle.dequant(q, scales_bits[:rows.size], zeros[:rows.size], group)
+    return tf_oracle.linear_f64(x_bits, wd)
+
+
+def _bad_rows_sorted(qweight, scales_bits, zeros, bits, group, K, x_bits, rows):
+    """Outputs in sorted (and de-duplicated) row order rather than the requested one."""
+    return tf_oracle.reference_rows(qweight, scales_bits, zeros, bits, group, K, x_bits, np.unique(rows))
+
+
+def _bad_reference_chunk_metadata(qweight, s, z, bits, group, K, x, rows_per_chunk=2048):
+    """Chunked over rows, but every chunk reads the first chunk's scales and zeros."""
+    n = qweight.shape[0]
+    y = np.empty((x.shape[0], n), dtype=np.float64)
+    for r0 in range(0, n, rows_per_chunk):
+        r1 = min(n, r0 + rows_per_chunk)
+        q = tf_oracle.unpack(qweight[r0:r1], bits, K)
+        wd = tf_oracle.dequant(q, s[:r1 - r0], z[:r1 - r0], group)
+        y[:, r0:r1] = tf_oracle.linear_f64(x, wd)
+    return y
+
+
 MUTANTS = {
+    "rows_metadata_by_position": dict(reference_rows=_bad_rows_metadata_by_position),
+    "rows_returned_sorted": dict(reference_rows=_bad_rows_sorted),
+    "reference_chunks_reuse_first_metadata": dict(reference=_bad_reference_chunk_metadata),
     "unpack_high_nibble_first": dict(unpack_w4=_bad_unpack_high_first),
     "dequant_sign_flipped": dict(dequant=_bad_dequant_sign),
     "dequant_prescaled_zero": dict(dequant=_bad_dequant_prescaled_zero),
