@@ -815,37 +815,6 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
 
 inline size_t gemv_scratch_bytes(const GemvPlan& P) { return P.slab ? 0 : P.partial_bytes + P.counter_bytes; }
 
-// Launch with programmatic dependent launch; opts the kernel in, once per
-// device, to the largest ring a plan can ask for.
-template <class Kern, class... Args>
-int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, int threads, int smem_max, size_t smem,
-               cudaStream_t s, Args... args) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
-  if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return TF_ERR_CUDA;
-    opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
-  }
-  if (smem > (size_t)smem_max) return TF_ERR_UNSUPPORTED;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kfn, args...) != cudaSuccess) {
-    cudaGetLastError();
-    return TF_ERR_CUDA;
-  }
-  return launch_status();
-}
-
 template <int BITS, int GPT>
 int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
   static std::atomic<unsigned long long> opted{0};
@@ -940,6 +909,11 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
   if (rc) return rc;
   if (M < 1) return TF_ERR_INVALID_ARG;
   if (M > 8) return TF_ERR_UNSUPPORTED;
+  StreamPlan SP;
+  if (stream_plan(G, M, &SP)) {
+    *bytes = 0;
+    return TF_OK;
+  }
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
@@ -961,6 +935,8 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
   if (M > 8) return TF_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(bias) & 1)) return TF_ERR_ALIGNMENT;
+  StreamPlan SP;
+  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, bias, y, M, stream);
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
@@ -1016,6 +992,8 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
   if (M > 8) return TF_ERR_UNSUPPORTED;
   if (!aligned16(x)) return TF_ERR_ALIGNMENT;
+  StreamPlan SP;
+  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, nullptr, y, M, stream);
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;

@@ -32,6 +32,17 @@ int encode_y_map(const uint16_t* y, int M, int N, CUtensorMap* map);
 // {unit/16, 2, 1, 8}.
 int encode_units_map(const uint8_t* units, int S, int KT, int unit_bytes, CUtensorMap* map);
 
+// The stream GEMV (gemv_stream.cu): M <= 8, at least one 16-row slab per
+// SM, groups of 64, any multiple of 128 or per channel; no workspace.
+// stream_plan returns 1 and fills *P when it takes the layer.
+struct StreamPlan {
+  int G, Mp, NS, npre, off_x, off_xs, off_red, off_ctl, max_slabs;
+  size_t smem;
+};
+int stream_plan(const Geometry& G, int M, StreamPlan* P);
+int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
+               uint16_t* y, int M, cudaStream_t stream);
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -67,6 +78,37 @@ inline int launch_status() {
   if (e == cudaSuccess) return TF_OK;
   cudaGetLastError();  // a launch error of ours is not sticky; clear it
   return TF_ERR_CUDA;
+}
+
+// Launch with programmatic dependent launch; opts the kernel in, once per
+// device, to the largest ring a plan can ask for.
+template <class Kern, class... Args>
+int launch_pdl(Kern kfn, std::atomic<unsigned long long>& opted, int grid, int threads, int smem_max, size_t smem,
+               cudaStream_t s, Args... args) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TF_ERR_CUDA;
+  if (!(opted.load(std::memory_order_acquire) & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return TF_ERR_CUDA;
+    opted.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+  if (smem > (size_t)smem_max) return TF_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kfn, args...) != cudaSuccess) {
+    cudaGetLastError();
+    return TF_ERR_CUDA;
+  }
+  return launch_status();
 }
 
 }  // namespace tf

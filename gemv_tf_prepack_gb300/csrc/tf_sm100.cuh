@@ -40,6 +40,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Arrive with an expected transaction count and no memory ordering: for a
+// stage whose earlier readers have already consumed their loaded values, so
+// that the arrive does not wait for this thread's outstanding global
+// operations (a release would).
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -62,6 +71,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0 && global_timer_ns() - t0 > timeout_ns) {
+      atomicCAS(err, 0u, code);
+      return false;
+    }
+  }
+}
+
+// try_wait that lets the hardware suspend the thread for up to hint_ns while
+// the phase is incomplete (fewer polling instructions than a bare try_wait).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with suspended polls (one thread waits for its warp).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, unsigned* err, unsigned code,
+                                                uint64_t timeout_ns) {
+  if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) {
       atomicCAS(err, 0u, code);
       return false;
     }

@@ -57,8 +57,9 @@ def test_gemv_small(N, K, bits, group, M):
     check_close(y, ref, f"gemv {N}x{K} w{bits} g{group} M={M}")
 
 
-# Layers with at least one 16-row slab per SM (and K >= 1024) take the slab
-# GEMV: whole slabs per CTA, K split over the CTA's warps, no workspace.
+# Layers with at least one 16-row slab per SM take the stream GEMV (groups of
+# 64, multiples of 128, per channel; M <= 8) or, for groups of 32, the slab
+# GEMV (whole slabs per CTA, K >= 1024, no workspace).
 SLAB_FORMATS = [
     (2440, 1016, 4, 0), (2440, 1152, 4, 128), (4104, 2048, 4, 32), (2432, 4096, 4, 64),
     (3000, 2048, 8, 0), (2560, 1280, 8, 64), (2448, 1024, 8, 32), (5000, 3072, 4, 128),
@@ -74,7 +75,7 @@ def _sms():
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_gemv_slab(N, K, bits, group, M):
     assert -(-N // 16) >= _sms() and -(-K // 128) >= 8, "shape meant for the slab GEMV"
-    if not (M == 8 and bits == 4 and group in (32, 64)):  # those stages do not fit twice per SM: tile GEMV
+    if not (M == 8 and bits == 4 and group == 32):  # those stages do not fit twice per SM: tile GEMV
         assert tf.gemv_workspace_size(N, K, bits, group, M) == 0
     qw, W = layer(N, K, bits, group, 23)
     xb = synth.make_activations(M, K, 23)
