@@ -404,14 +404,15 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   // publishes everything.
   {
     const int hw = lane >> 4, r = lane & 15;
+    const int hid = warp * 2 + hw;  // half warp of the CTA
     const int nblk = KT * a.M;
     constexpr int kBatch = 4;  // blocks per half warp whose loads are in flight together
-    for (int base = warp * 2 * kBatch; base < nblk; base += 2 * kSW * kBatch) {  // uniform over the warp
-      const int b0 = base + hw * kBatch;
+    // blocks hid, hid + 32, hid + 64, ... (every half warp busy, loads batched)
+    for (int base = 0; base < nblk; base += 2 * kSW * kBatch) {  // uniform over the warp
       uint4 v[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        const int b = b0 + q;
+        const int b = base + q * 2 * kSW + hid;
         const int kt = ONE ? b : b / a.M, m = ONE ? 0 : b - kt * a.M;
         const int col = kt * kTileK + 8 * r;
         v[q] = make_uint4(0, 0, 0, 0);
@@ -419,7 +420,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
       }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        const int b = b0 + q;  // uniform over the half warp
+        const int b = base + q * 2 * kSW + hid;  // uniform over the half warp
+        if (base + q * 2 * kSW >= nblk) break;   // uniform over the warp
         uint32_t E = chunk_max_exponent(v[q]);
 #pragma unroll
         for (int d = 1; d < 16; d <<= 1) E = max(E, __shfl_xor_sync(0xFFFFFFFFu, E, d));
