@@ -66,7 +66,7 @@ struct GemmArgs {
   unsigned* err;              // device error word
   float* ws;                  // stream-K partial sums: [CTA][2][BN / 16][128 rows][16]
   unsigned* cnt;              // stream-K arrivals per tile (zero on entry and on exit)
-  int N, K, M, KT, g, tile_bytes;  // tile_bytes: one packed tile (eight units) in shared memory
+  int N, K, M, KT, g, group, tile_bytes;  // tile_bytes: one packed tile (eight units) in shared memory
   int MT, BN, ntiles;
   int dp_tiles;               // tiles [0, dp_tiles) whole per CTA; the rest split along K
   int sk_ctas;                // CTAs [0, sk_ctas) share the split tiles' k-iterations (at least one each)
@@ -298,6 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
     volatile unsigned* flag = reinterpret_cast<volatile unsigned*>(smem + (B.flag - sbase));
+    // The only writers check the blob's header: with one that does not
+    // describe this layer they drain every accumulator but write nothing
+    // (no y, no partial sums, no arrival counts).
+    uint4 h0, h1;
+    load_header(a.units, h0, h1);
+    const bool write = header_matches(h0, h1, a.N, a.K, BITS, a.group);
+    if (!write && row == 0 && blockIdx.x == 0) atomicCAS(err, 0u, kErrBlobHeader);
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const bool whole = wk.kb == 0 && wk.ke == a.KT;
       const int ti = wk.tile - a.dp_tiles;
       float* mine = whole ? nullptr : sk_slot(a, blockIdx.x, ti);
-      for (int c0 = 0; c0 < a.BN; c0 += 16) {
+      for (int c0 = 0; c0 < a.BN && write; c0 += 16) {
         uint32_t r[16];
         tmem_ld_16(taddr + (uint32_t)c0, r);
         tmem_ld_wait();
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(B.tempty + 8 * acc);
       if (++acc == 2) { acc = 0; aph ^= 1; }
-      if (whole) continue;
+      if (whole || !write) continue;
       // stream-K segment: publish the partial sums, count this contribution
       fence_acq_rel_gpu();
       named_barrier_sync(kEpilogueThreads);
@@ -541,7 +548,8 @@ struct GemmPlan {
 // along K; needs the workspace sized by ws_bytes + cnt_bytes.
 int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
   GemmArgs& a = P->a;
-  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.tile_bytes = kSlabsPerTile * G.unit_bytes;
+  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
+  a.tile_bytes = kSlabsPerTile * G.unit_bytes;
   a.BN = M >= 256 ? 256 : (M + 15) / 16 * 16;
   a.MT = (M + a.BN - 1) / a.BN;
   a.ntiles = G.NB * a.MT;

@@ -37,7 +37,8 @@ namespace {
 
 template <int BITS, int GPT>
 __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict__ units, int N, int K,
-                                                      int KT, int g, uint16_t* __restrict__ w) {
+                                                      int KT, int g, int group, unsigned* err,
+                                                      uint16_t* __restrict__ w) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
   constexpr int SB = BITS == 4 ? 16 : 32;
   const int tile = blockIdx.x;
@@ -76,6 +77,13 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
       lo[2 * j] = a[0]; lo[2 * j + 1] = a[2];
       hi[2 * j] = a[1]; hi[2 * j + 1] = a[3];
     }
+  }
+  // a blob whose header describes another layer: write nothing
+  uint4 h0, h1;
+  load_header(units, h0, h1);
+  if (!header_matches(h0, h1, N, K, BITS, group)) {
+    if (threadIdx.x == 0 && tile == 0) atomicCAS(err, 0u, kErrBlobHeader);
+    return;
   }
   const int n0 = nb * kTileN + mb * kSlabN + gr;
   const int k0 = kt * kTileK + h * 64 + 16 * t;
@@ -250,7 +258,7 @@ struct GemvArgs {
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
   unsigned* err;
   long long T;
-  int N, K, M, KT, g, G, S_max;
+  int N, K, M, KT, g, G, S_max, group;
   int NS, stage_bytes, x_off;  // shared-memory ring: stages, bytes per stage, x slice offset
 };
 
@@ -390,8 +398,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   const uint32_t empty = full + 8u * a.NS;
   // per-stage release counters: the last warp to hand a stage back refills it
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.NS * a.stage_bytes + 16 * a.NS);
+  int* bad = reinterpret_cast<int*>(released + a.NS);  // the blob's header does not match the call
   const int npre = nfill < a.NS ? nfill : a.NS;
+  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
   if (threadIdx.x == 0) {
+    load_header(a.units, h0, h1);  // compared below, once the grid dependency has resolved
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full + 8 * i, 1);
       mbar_init(empty + 8 * i, kGemvWarps);
@@ -412,9 +423,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   }
   // y, x and the workspace may still be in use by the previous grid
   griddep_wait();
+  if (threadIdx.x == 0) {
+    *bad = header_matches(h0, h1, a.N, a.K, BITS, a.group) ? 0 : 1;
+    if (*bad) atomicCAS(a.err, 0u, kErrBlobHeader);
+  }
   if (warp == 0)
     for (int f = 0; f < npre; ++f)
       issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true, lane);
+  __syncthreads();
+  // With a header that does not match, the stream still runs to the end (so
+  // that every copy lands) but nothing is written.
+  const bool write = *bad == 0;
 
   const int gr = lane >> 2, t = lane & 3;  // mma.sync fragment coordinates
   (void)gr;
@@ -460,7 +479,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
         if (i0 + j == seg.end) {
           const float v[4] = {acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
                               acc[0][3] + acc[1][3]};
-          if (end_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v)) {
+          if (write && end_segment(a, c, t0, seg.nb, seg.whole, warp, lane, v)) {
             if (npending == 0) pending0 = seg.nb; else pending1 = seg.nb;
             ++npending;
           }
@@ -512,7 +531,7 @@ struct SlabArgs {
   uint16_t* y;
   const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
   unsigned* err;
-  int N, K, M, KT, g;
+  int N, K, M, KT, g, group;
   int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
   int NS, stage_bytes, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
 };
@@ -586,7 +605,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
   float2* red2 = reinterpret_cast<float2*>(red);               // M = 1: [spc slabs][8 warps][8 rows]
   const int tq = (a.M + 1) >> 1;  // lanes per row group holding real tokens (2t, 2t + 1)
   const int npre = nfill < a.NS ? nfill : a.NS;
+  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
   if (threadIdx.x == 0) {
+    load_header(a.units, h0, h1);  // compared below, before anything is written
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full + 8 * i, 1);
       released[i] = 0;
@@ -610,6 +631,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
   if (warp == 0)
     for (int f = 1; f < npre; ++f) slab_fill<BITS, GPT, NW>(a, sbase, full, s0, f, f, lane);
   cp_async_wait_all();
+  if (threadIdx.x == 0 && !header_matches(h0, h1, a.N, a.K, BITS, a.group)) {
+    ctl[1] = 1;  // write nothing; the stream still runs, so that every copy lands
+    atomicCAS(a.err, 0u, kErrBlobHeader);
+  }
   __syncthreads();
 
   const LaneOffsets o = lane_offsets<BITS, GPT>(lane, a.g, a.M);
@@ -625,7 +650,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
   const int last_n = a.KT - (a.QPS - 1) * U;  // units in the last stage of a slab (1..U)
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   WRegs<BITS, GPT> R[UPW];
-  bool dead = false;  // a wait ran out: stop computing, keep the bookkeeping going
+  bool dead = ctl[1] != 0;  // a wait ran out (or a bad header): stop computing, keep the bookkeeping going
   int st = 0, q = 0, si = 0;
   uint32_t lap = 0;
   const uint8_t* stp = smem;                         // stage st
@@ -809,7 +834,7 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   P->x_off = (TPS * kSlabsPerTile * Gm.unit_bytes + 127) / 128 * 128;
   P->stage_bytes = P->x_off + TPS * M * 256;
   P->NS = clampi(kGemvSmemBudget / P->stage_bytes, 2, 6);
-  P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS;
+  P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS + 4;
   return TF_OK;
 }
 
@@ -838,7 +863,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
   if (P.slab) {
     SlabArgs a;
     a.units = units; a.x = x; a.y = y; a.bias = bias; a.err = err;
-    a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
+    a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
     a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS;
     a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.xres_off = P.xres_off;
     a.red_off = P.red_off; a.ctl_off = P.ctl_off;
@@ -857,7 +882,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
   GemvArgs a;
   a.units = units; a.y = y; a.bias = bias; a.partials = partials; a.counters = counters; a.err = err;
   a.T = P.T;
-  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g;
+  a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
   a.G = P.G; a.S_max = P.S_max;
   a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.x_off = P.x_off;
   if (G.bits == 4) {
@@ -871,8 +896,8 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
 }
 
 template <int BITS, int GPT>
-void launch_dequant(const uint8_t* units, const Geometry& G, uint16_t* w, cudaStream_t s) {
-  dequant_kernel<BITS, GPT><<<G.NB * G.KT, 512, 0, s>>>(units, G.N, G.K, G.KT, G.g, w);
+void launch_dequant(const uint8_t* units, const Geometry& G, unsigned* err, uint16_t* w, cudaStream_t s) {
+  dequant_kernel<BITS, GPT><<<G.NB * G.KT, 512, 0, s>>>(units, G.N, G.K, G.KT, G.g, G.group, err, w);
 }
 
 }  // namespace
@@ -890,14 +915,16 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
   if (!w) return TF_ERR_INVALID_ARG;
   if (!aligned16(w)) return TF_ERR_ALIGNMENT;
   const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  unsigned* err = device_error_ptr();
+  if (!err) return TF_ERR_CUDA;
   if (bits == 4) {
-    if (G.gpt == 1) launch_dequant<4, 1>(units, G, w, stream);
-    else if (G.gpt == 2) launch_dequant<4, 2>(units, G, w, stream);
-    else launch_dequant<4, 4>(units, G, w, stream);
+    if (G.gpt == 1) launch_dequant<4, 1>(units, G, err, w, stream);
+    else if (G.gpt == 2) launch_dequant<4, 2>(units, G, err, w, stream);
+    else launch_dequant<4, 4>(units, G, err, w, stream);
   } else {
-    if (G.gpt == 1) launch_dequant<8, 1>(units, G, w, stream);
-    else if (G.gpt == 2) launch_dequant<8, 2>(units, G, w, stream);
-    else launch_dequant<8, 4>(units, G, w, stream);
+    if (G.gpt == 1) launch_dequant<8, 1>(units, G, err, w, stream);
+    else if (G.gpt == 2) launch_dequant<8, 2>(units, G, err, w, stream);
+    else launch_dequant<8, 4>(units, G, err, w, stream);
   }
   return launch_status();
 }

@@ -70,7 +70,6 @@ constexpr int kSmemMax = 227 * 1024;  // one CTA per SM
 constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr unsigned kErrStreamWait = 0x700;
-constexpr unsigned kErrStreamHeader = 0x800;
 
 // Units per stage of a warp's ring (one bulk copy): 4 INT4 or 2 INT8 units,
 // about 4 KB.
@@ -377,9 +376,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   if (threadIdx.x == 0) {
     // the header of the blob, compared with the call's arguments before
     // anything is written (see below)
-    const uint4* hp = reinterpret_cast<const uint4*>(a.units - kHeaderBytes);
-    h0 = __ldg(hp);
-    h1 = __ldg(hp + 1);
+    load_header(a.units, h0, h1);
     for (int i = 0; i < kSW * NS; ++i) mbar_init(full + 8 * i, 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -456,13 +453,11 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
     }
   }
   if (threadIdx.x == 0) {
-    const bool ok = h0.x == kMagic && h0.y == kVersion && (int)h0.z == a.N && (int)h0.w == a.K &&
-                    (int)h1.x == BITS && (int)h1.y == a.group;
-    flags[1] = ok ? 0 : 1;
+    flags[1] = header_matches(h0, h1, a.N, a.K, BITS, a.group) ? 0 : 1;
   }
   __syncthreads();
   bool dead = flags[1] != 0;  // a header that does not match: write nothing
-  if (dead && threadIdx.x == 0) atomicCAS(a.err, 0u, kErrStreamHeader);
+  if (dead && threadIdx.x == 0) atomicCAS(a.err, 0u, kErrBlobHeader);
   // x is in: the rest of the rings follows (requested earlier, these stages
   // would have reached the SM ahead of the activations)
   int issued = npre;  // stages of this warp requested so far

@@ -117,6 +117,26 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 }
 
 // ---------------------------------------------------------------------------
+// blob header check
+
+// Device error code of a call whose blob header does not describe the layer
+// the call names (another layer's blob of the same size, a stale blob).
+constexpr unsigned kErrBlobHeader = 0x800;
+
+// True when the 64-byte header in front of `units` carries the magic, the
+// format version and (N, K, bits, group) of the call.
+__device__ __forceinline__ bool header_matches(const uint4 h0, const uint4 h1, int N, int K, int bits, int group) {
+  return h0.x == kMagic && h0.y == kVersion && (int)h0.z == N && (int)h0.w == K && (int)h1.x == bits &&
+         (int)h1.y == group;
+}
+
+__device__ __forceinline__ void load_header(const uint8_t* units, uint4& h0, uint4& h1) {
+  const uint4* hp = reinterpret_cast<const uint4*>(units - kHeaderBytes);
+  h0 = __ldg(hp);
+  h1 = __ldg(hp + 1);
+}
+
+// ---------------------------------------------------------------------------
 // loads
 
 // Streamed once: no L1 allocation.

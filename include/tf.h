@@ -33,6 +33,10 @@
  *    TF_ERR_CUDA return means the launch itself failed.
  *  - Calls are thread-safe.  Two device calls that share a workspace must
  *    not run concurrently.
+ *  - The host checks blob_bytes against (N, K, bits, group); the kernels also
+ *    read the device blob's 64-byte header and, when it describes another
+ *    layer (for instance a blob of the same size with N and K swapped), write
+ *    nothing and record 0x800 in the device error word (tf_device_error).
  */
 #ifndef TF_H_
 #define TF_H_
@@ -45,7 +49,8 @@
 extern "C" {
 #endif
 
-#define TF_VERSION 3  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias */
+#define TF_VERSION 4  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias; 4: tf_gemv_noalloc,
+                         TF_ERR_SCRATCH_LIMIT, device-side check of the blob header */
 
 #define TF_OK 0
 #define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */
@@ -139,26 +144,36 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
 
 /*
  * Workspace bytes tf_gemv needs on the current device for this layer and M
- * (split-K partial sums plus per-block arrival counters; 0 for layers whose
- * blocks each stream whole 16-row slabs).  The workspace must be
- * zero-filled before its first use; every tf_gemv leaves the arrival
- * counters at zero again (the partial sums are always written before they
- * are read), so one workspace can be reused by calls ordered on one stream.
+ * (split-K partial sums plus per-block arrival counters; 0 for layers with
+ * at least one 16-row slab per SM, whose blocks each stream whole slabs).
+ * The workspace must be zero-filled before its first use; every tf_gemv
+ * that completes leaves the arrival counters at zero again (the partial sums
+ * are always written before they are read), so one workspace can be reused
+ * by calls ordered on one stream.  After a call that reported a device error
+ * (tf_device_error nonzero) zero the workspace again before reusing it.
  */
 int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
 /*
  * Fused GEMV for token generation ("GEMV dataflow co-design", Methodology 3;
  * batch 1, and up to 8 rows at no extra cost): y[M, N] = x[M, K] * W^T.
- * Each weight code is read from HBM once, unpacked and dequantised to BF16 in
- * registers and fed straight to the tensor cores (mma.sync, FP32
- * accumulation), with the whole chip streaming weights.  Layers with at
- * least one 16-row slab per SM (and K >= 1024) give every block whole slabs
- * and split K over the block's warps, with x resident in shared memory; the
- * others (few rows, short K, or x too large to stay resident) split K across
- * all blocks, and the last-arriving block of each row block adds the partial
- * sums.  Every addition happens in a fixed order, so results are
- * deterministic run to run.
+ * Each weight code is read from HBM once, unpacked in registers and fed
+ * straight to the tensor cores (mma.sync, FP32 accumulation), with the whole
+ * chip streaming weights.
+ *  - Layers with at least one 16-row slab per SM and groups of 64, multiples
+ *    of 128 or per channel: every block owns whole slabs, each warp streams
+ *    a contiguous run of them.  The codes enter the tensor cores exactly (as
+ *    FP16), x is converted to FP16 with a power-of-two scale per 128-column
+ *    block (exact), and (q - z) * s is applied per group in FP32 to the
+ *    sums: the result is sum_k x * (q - z) * s without rounding each
+ *    dequantised weight to BF16 (tf_dequant and tf_gemm keep that rounding).
+ *  - Groups of 32 on such layers: whole slabs per block, K split over the
+ *    block's warps, each weight dequantised to BF16 in registers as above.
+ *  - The others (few rows, or x too large to stay resident): K split across
+ *    all blocks, the last-arriving block of each row block adding the
+ *    partial sums.
+ * Every addition happens in a fixed order, so results are deterministic run
+ * to run.
  * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),
  * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size; may
  * be NULL when that is 0).  1 <= M <= 8, else TF_ERR_UNSUPPORTED.
@@ -241,7 +256,10 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
  * Read and clear the current device's error word (synchronous).  Kernels
  * that wait on on-chip barriers give up after a bounded time instead of
  * hanging, set a nonzero code here and exit; *code receives 0 if nothing
- * went wrong since the last read.
+ * went wrong since the last read.  Codes: 0x100-0x500 a GEMM wait ran out
+ * (producer, dequant, MMA, epilogue, drain), 0x600 a tile or slab GEMV wait,
+ * 0x700 a stream GEMV wait, 0x800 the device blob's header does not match
+ * the call (nothing written).  The first code since the last read is kept.
  */
 int tf_device_error(unsigned int* code);
 

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol():
     lib = tf.lib()
     for d in decl:
         getattr(lib, d)
-    assert tf.version() == 3
+    assert tf.version() == 4
 
 
 @pytest.mark.parametrize("N,K,bits,group", [
@@ -105,8 +105,10 @@ def test_invalid_arguments_return_codes():
     short = out[:-16]
     with pytest.raises(tf.TFError):
         tf.unprepack(short)
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert lib.tf_status_string(code)
+    assert lib.tf_status_string(-8).decode().startswith("TF_ERR_SCRATCH_LIMIT")
+    assert lib.tf_status_string(-5).decode().startswith("TF_ERR_BAD_BLOB")
 
 
 def test_device_calls_validate_before_touching_the_gpu():

@@ -304,3 +304,45 @@ def test_symmetric_zero_point(N, K, bits, group):
         xb = synth.make_activations(M, K, 53)
         ref = tf_oracle.reference(qw.qweight, qw.scales, zeros, bits, group, K, xb)
         check_close(to_host_bits(fn(W, to_dev_bf16(xb))), ref, f"symmetric {fn.__name__} {N}x{K} w{bits} M={M}")
+
+
+# (call, described layer (N, K, bits, group), the other layer's shape, M): both
+# layers have the same number of units, so the blob sizes agree and only the
+# header can tell them apart.
+HEADER_CASES = [
+    ("gemv", (1024, 2048, 4, 128), (2048, 1024), 1),   # tile GEMV (fewer slabs than SMs)
+    ("gemv", (4096, 2048, 4, 32), (2048, 4096), 1),    # slab GEMV (groups of 32)
+    ("gemm", (4096, 11008, 4, 128), (11008, 4096), 64),
+    ("gemm", (4096, 11008, 4, 128), (11008, 4096), 300),
+    ("gemm_whole", (4096, 11008, 4, 128), (11008, 4096), 300),
+    ("dequant", (1024, 2048, 4, 128), (2048, 1024), 0),
+]
+
+
+@pytest.mark.parametrize("call,desc,other,M", HEADER_CASES, ids=[f"{c[0]}-{c[1][0]}x{c[1][1]}-M{c[3]}" for c in HEADER_CASES])
+def test_mismatched_header_rejected_on_device(call, desc, other, M):
+    """A device blob of another layer with the same size: the kernel reads its
+    header, records 0x800 in the device error word and writes nothing (y and
+    the stream-K workspace stay as they were)."""
+    import torch
+    N, K, bits, group = desc
+    _, Wo = layer(other[0], other[1], bits, group, 51)
+    assert Wo.nbytes == tf.prepack_size(N, K, bits, group)
+    wrong = tf.Weights(Wo.blob, N, K, bits, group)
+    assert tf.device_error() == 0
+    if call == "dequant":
+        out = torch.full((N, K), 3.0, dtype=torch.bfloat16, device="cuda")
+        tf.dequant(wrong, out=out)
+    else:
+        x = to_dev_bf16(synth.make_activations(M, K, 51))
+        out = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        if call == "gemv":
+            tf.gemv(wrong, x, out)
+        else:
+            tf.gemm(wrong, x, out, stream_k=(call == "gemm"))
+    torch.cuda.synchronize()
+    assert tf.device_error() == 0x800
+    assert bool((out == 3.0).all()), "a mismatched blob must not be written through"
+    if call == "gemm":
+        ws = wrong.workspace(M, "gemm")
+        assert int(ws.view(torch.uint8).sum()) == 0
