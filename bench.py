@@ -11,7 +11,11 @@ AWQ-style min/max recipe and BF16 activations.
 Timing: W untimed warm-up steps, then K steps replayed from CUDA graphs on
 one stream, bracketed by CUDA events with a device synchronisation on both
 sides; the GEMV step rotates through weight copies totalling more than 3x
-the L2 size so that every launch streams its weights from HBM.
+the L2 size so that every launch streams its weights from HBM.  Next to the
+headline the same run reports the square 8192 x 8192 layers (W8 per channel
+and W4 g64 at M = 1, 8, 64) and the large W4 g128 layers at M = 1, each as
+us per launch, GB/s and fraction of the measured HBM copy bandwidth, and
+the float64 oracle on all host cores (a process pool over output rows).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -38,6 +42,10 @@ DECODE = [(12288, 4096, 1), (4096, 4096, 2), (22016, 4096, 3), (4096, 11008, 4)]
 PREFILL = [(11008, 4096, 7), (4096, 11008, 8), (12288, 4096, 9)]
 PREFILL_M = 2048
 BITS, GROUP = 4, 128
+# (name, N, K, bits, group, seed, M list): square layers and the large-dimension layers
+SQUARE = [("w8_per_channel", 8192, 8192, 8, 0, 5, (1, 8, 64)), ("w4_g64", 8192, 8192, 4, 64, 6, (1, 8, 64))]
+LARGE = [("32768x8192", 32768, 8192, 4, 128, 10, (1,)), ("8192x32768", 8192, 32768, 4, 128, 11, (1,)),
+         ("32768x32768", 32768, 32768, 4, 128, 12, (1,))]
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -65,7 +73,7 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-GEMV_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemv.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
+GEMV_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemv_stream.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
                 "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
 GEMM_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemm.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
                 "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
@@ -231,6 +239,70 @@ def job_rate(units_per_rank: float, world: int, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
+def time_launches(torch, fn, Ws, x, y, stream):
+    """us per launch of fn over the weight copies Ws, back to back in one CUDA
+    graph (the copies together exceed the L2 size), timed with CUDA events
+    after warm-up replays."""
+    with torch.cuda.stream(stream):
+        for W in Ws:
+            fn(W, x, y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for W in Ws:
+            fn(W, x, y)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    reps = max(5, min(500, int(0.2e3 / max(e0.elapsed_time(e1), 1e-3))))  # about 0.2 s
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(Ws))
+
+
+def extra_layers(torch, tf, synth, stream, hbm_peak, peak_src):
+    """The square 8192^2 layers (W8 per channel, W4 g64) at M = 1, 8, 64 and
+    the large W4 g128 layers at M = 1: us per launch, GB/s of algorithmic
+    bytes and the fraction of the measured HBM copy bandwidth (all of these
+    are bound by HBM: flop/byte <= 224 at M = 64)."""
+    out = {}
+    for group_name, cases in (("square_8192", SQUARE), ("large_m1", LARGE)):
+        res = {}
+        for name, N, K, bits, group, seed, Ms in cases:
+            qw = synth.make_weights(N, K, bits, group, seed)
+            blob = tf.prepack(qw.qweight, qw.scales, qw.zeros, N, K, bits, group)
+            copies = max(2, int(np.ceil(3 * L2_BYTES / blob.size)) + 1)
+            Ws = [tf.Weights.upload(blob) for _ in range(copies)]
+            for M in Ms:
+                xb = synth.make_activations(M, K, seed)
+                x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+                y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+                call = tf.gemv if M <= 8 else tf.gemm
+
+                def fn(W, x, y, call=call):
+                    call(W, x, y, stream=stream)
+
+                us = time_launches(torch, fn, Ws, x, y, stream)
+                gbs = algo_bytes(M, N, K, bits, group) / (us * 1e-6) / 1e9
+                res[f"{name}_M{M}"] = {"call": call.__name__, "us": round(us, 2), "GB/s": round(gbs, 1),
+                                       "frac": round(gbs / hbm_peak, 4), "TFLOP/s": round(2.0 * M * N * K / us / 1e6, 2)}
+            del Ws
+            torch.cuda.empty_cache()
+        out[group_name] = res
+    out["peak"] = {"hbm_gbs": hbm_peak, "source": peak_src}
+    out["l2"] = "each layer rotates through weight copies totalling more than 3x L2; one CUDA graph per layer"
+    return out
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -350,7 +422,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     psingles = [capture_step(torch, gemm_call, pre, r, stream, [None] * (len(PREFILL) + 1)) for r in range(pcopies)]
     pbig = capture_steps(torch, gemm_call, pre, pcopies, stream)
-    psteps = max(args.steps // 20, 10)
+    psteps = args.steps  # the same step count as the decode step
     with torch.cuda.stream(stream):
         replay_steps(pbig, psingles, pcopies, args.warmup, stream)
     torch.cuda.synchronize()
@@ -379,6 +451,12 @@ def run_ours(args, rank, world):
     tc_ref = tc_peak_sus if long_region else tc_peak
     pclocks = pclk.summary()
 
+    for L in pre:
+        L["Ws"].clear(); L["xs"].clear(); L["ys"].clear()
+    del psingles, pbig, piso
+    torch.cuda.empty_cache()
+    extras = None if args.no_extras else extra_layers(torch, tf, synth, stream, hbm_peak, peak_src)
+
     err = tf.device_error()
     if rank != 0:
         return None
@@ -405,8 +483,8 @@ def run_ours(args, rank, world):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-            "traffic": recorded_traffic("gemv_slab_kernel", GEMV_SOURCES),
-            "kernel": "gemv_slab_kernel<4,1>", "algorithmic_bytes_per_launch": round(per_launch_bytes),
+            "traffic": recorded_traffic("gemv_stream_kernel", GEMV_SOURCES),
+            "kernel": "gemv_stream_kernel<4, 1, 1>", "algorithmic_bytes_per_launch": round(per_launch_bytes),
             "kernel_us_per_launch": round(kernel_ms * 1e3, 3),
             "isolated_launch_us": iso_us,
         },
@@ -429,6 +507,8 @@ def run_ours(args, rank, world):
         "clocks": clocks,
         "device_error": err,
     }
+    if extras is not None:
+        line["layers"] = extras
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     return line
@@ -437,70 +517,122 @@ def run_ours(args, rank, world):
 # ---------------------------------------------------------------------------
 # CPU oracle (the reference arm and the cpu_baseline leg)
 
-CPU_SAMPLE_ROWS = 256
+CPU_SAMPLE_ROWS = 2048  # output rows of each decode projection in the CPU baseline's sample
 
 
-def _oracle_sample_cmd():
-    return [sys.executable, os.path.abspath(__file__), "--oracle-sample"]
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
-def oracle_sample() -> dict:
-    """Time the oracle on the first 256 output rows of each decode projection."""
-    from gemv_tf_prepack_gb300 import synth
+def _oracle_worker(job):
+    """One worker's share: the oracle on a block of output rows (float64)."""
     from oracle import tf_oracle
+
+    qw, sc, z, x, K = job
+    t = time.perf_counter()
+    tf_oracle.reference(qw, sc, z, BITS, GROUP, K, x)
+    return time.perf_counter() - t
+
+
+def _oracle_sample(rows):
+    """The first `rows` output rows of each decode projection (the same
+    generator stream as the full layers) and its activations."""
+    from gemv_tf_prepack_gb300 import synth
 
     data = []
     for N, K, seed in DECODE:
         rng = np.random.default_rng(seed)
-        w = rng.standard_normal((CPU_SAMPLE_ROWS, K), dtype=np.float32) * np.float32(0.02)
-        qw = synth.quantise(w, BITS, GROUP)
-        data.append((qw, synth.make_activations(1, K, seed)))
-    t = time.perf_counter()
+        w = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(0.02)
+        data.append((synth.quantise(w, BITS, GROUP), synth.make_activations(1, K, seed)))
+    return data
+
+
+def _oracle_jobs(data, r0, r1, cores):
+    jobs = []
     for qw, x in data:
-        tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, BITS, GROUP, qw.K, x)
-    dt = time.perf_counter() - t
-    nbytes = sum(algo_bytes(1, CPU_SAMPLE_ROWS, qw.K) for qw, _ in data)
-    return {"seconds": dt, "bytes": nbytes}
+        for c in range(cores):
+            a, b = r0 + (r1 - r0) * c // cores, r0 + (r1 - r0) * (c + 1) // cores
+            if b > a:
+                jobs.append((qw.qweight[a:b], qw.scales[a:b], qw.zeros[a:b], x, qw.K))
+    return jobs
 
 
-def cpu_baseline(reps: int = 1) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    env.pop("RANK", None)
-    env.pop("WORLD_SIZE", None)
-    secs, nbytes = 0.0, 0.0
-    for _ in range(reps):
-        out = subprocess.run(_oracle_sample_cmd(), capture_output=True, text=True, env=env, cwd=ROOT)
-        rec = json.loads(out.stdout.strip().splitlines()[-1])
-        secs += rec["seconds"]
-        nbytes += rec["bytes"]
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"unpack + dequant + float64 product of the first {CPU_SAMPLE_ROWS} output rows of each "
-                      "of the 4 decode projections (M=1), one process, BLAS threads = 1"}
+class OraclePool:
+    """The float64 oracle on every host core: a spawn-started process pool
+    (one single-threaded BLAS per worker) over blocks of output rows."""
+
+    def __init__(self):
+        import multiprocessing as mp
+
+        self.cores = _host_cores()
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"  # inherited by the workers
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+
+    def run(self, data, r0, r1):
+        """Wall-clock seconds and algorithmic bytes of rows [r0, r1) of every projection."""
+        jobs = _oracle_jobs(data, r0, r1, self.cores)
+        t = time.perf_counter()
+        self.pool.map(_oracle_worker, jobs, chunksize=1)
+        dt = time.perf_counter() - t
+        return dt, sum(algo_bytes(1, r1 - r0, qw.K) for qw, _ in data)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline() -> dict:
+    data = _oracle_sample(CPU_SAMPLE_ROWS)
+    op = OraclePool()
+    try:
+        op.run(data, 0, CPU_SAMPLE_ROWS)  # workers started and their memory touched before timing
+        runs = [op.run(data, 0, CPU_SAMPLE_ROWS) for _ in range(3)]
+    finally:
+        op.close()
+    secs = statistics.median(r[0] for r in runs)
+    nbytes = runs[0][1]
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": op.cores, "kind": "oracle",
+            "blas_threads_per_worker": 1,
+            "sample": f"unpack + dequant + float64 product of the first {CPU_SAMPLE_ROWS} output rows of each of "
+                      f"the 4 decode projections (M=1), split over {op.cores} spawn-started worker processes "
+                      "(all host cores, one BLAS thread each); median of 3 after a warm-up pass"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    times, nbytes = [], None
-    for s in range(args.warmup + args.steps):
-        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-        for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
-            env.pop(k, None)
-        out = subprocess.run(_oracle_sample_cmd(), capture_output=True, text=True, env=env, cwd=ROOT)
-        rec = json.loads(out.stdout.strip().splitlines()[-1])
-        if s >= args.warmup:
-            times.append(rec["seconds"])
-            nbytes = rec["bytes"]
-    sec = sum(times) / len(times)
+    data = _oracle_sample(CPU_SAMPLE_ROWS)
+    op = OraclePool()
+    steps = args.warmup + args.steps
+    # each step a slice of the sample, sized so that the whole run stays
+    # within a few minutes whatever the step count
+    per = max(op.cores, min(CPU_SAMPLE_ROWS, (16 * CPU_SAMPLE_ROWS) // steps))
+    times, nbytes = [], 0.0
+    try:
+        op.run(data, 0, CPU_SAMPLE_ROWS)  # workers started and their memory touched before timing
+        for s in range(steps):
+            r0 = (s * per) % CPU_SAMPLE_ROWS
+            r1 = min(CPU_SAMPLE_ROWS, r0 + per)
+            dt, nb = op.run(data, r0, r1)
+            if s >= args.warmup:
+                times.append(dt)
+                nbytes += nb
+    finally:
+        op.close()
+    sec = sum(times)
     value = nbytes / sec / 1e9
-    sample = (f"oracle (float64 CPU reference): first {CPU_SAMPLE_ROWS} output rows of each of the 4 decode "
-              "projections per step, one process, BLAS threads = 1")
+    sample = (f"oracle (float64 CPU reference) on {op.cores} worker processes (all host cores, one BLAS thread each): "
+              f"{per} output rows of each of the 4 decode projections per step")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "decode step: 4 Llama-7B-like W4A16 g128 projections at M=1 (row sample)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": op.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -546,14 +678,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--no-extras", action="store_true", help="skip the square and large layer measurements")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
                     help="run one workload's launches a few times, untimed (for ncu captures)")
     ap.add_argument("--profile-reps", type=int, default=2)
     args = ap.parse_args()
-    if args.oracle_sample:
-        print(json.dumps(oracle_sample()))
-        return
     if args.profile:
         run_profile(args.profile, args.profile_reps)
         return

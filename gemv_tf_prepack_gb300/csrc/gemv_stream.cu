@@ -72,8 +72,8 @@ constexpr uint64_t kDrainNs = 200000000ull;
 constexpr unsigned kErrStreamWait = 0x700;
 
 // Units per stage of a warp's ring (one bulk copy): 4 INT4 or 2 INT8 units,
-// about 4 KB.
-__host__ __device__ constexpr int warp_stage_units(int bits) { return bits == 4 ? 4 : 2; }
+// about 4 KB, or half that when large activations leave less room.
+__host__ __device__ constexpr int warp_stage_units(int bits, bool half) { return (bits == 4 ? 4 : 2) / (half ? 2 : 1); }
 
 struct StreamArgs {
   const uint8_t* units;  // the blob's units (after the header)
@@ -85,7 +85,8 @@ struct StreamArgs {
   int N, K, M, Mp, KT, G, group;
   int NS, npre;          // per-warp ring: stages, stages requested before the grid dependency resolves
   int off_x, off_xs, off_red, off_ctl;  // byte offsets in the 128-aligned dynamic shared memory
-  int max_slabs;         // slabs of the busiest CTA (sizes the parked sums)
+  int max_slabs;         // slabs of the busiest CTA
+  int compact;           // parked sums: 1 = two slots per warp, 0 = one slot per (slab, warp)
 };
 
 // The run of units of warp w of a CTA whose units are [u0, u1).
@@ -323,26 +324,17 @@ __device__ __forceinline__ void store_out(const StreamArgs& a, int bits, int tok
   a.y[(size_t)tok * a.N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(out));
 }
 
-// The sixteen warps' parked sums of one output (stride `per` floats), added
-// in warp order.
-__device__ __forceinline__ float sum_warps(const float* rr, int per) {
-  float v = 0.f;
-#pragma unroll
-  for (int w = 0; w < kSW; ++w) v += rr[w * per];
-  return v;
-}
-
 // ---------------------------------------------------------------------------
 // the kernel
 
-template <int BITS, int GPT, bool ONE>
+template <int BITS, int GPT, bool ONE, bool HALF>
 __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // 128-byte alignment by offsetting the array itself (not through an integer
   // cast), so that every access below stays a shared-memory access
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
-  constexpr int S = warp_stage_units(BITS);
+  constexpr int S = warp_stage_units(BITS, HALF);
   constexpr int SB = S * UB;  // bytes of a stage
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t = lane & 3;
@@ -357,7 +349,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   const uint32_t sbase = smem_u32(smem);
   uint8_t* xres = smem + a.off_x;
   float* xsum = reinterpret_cast<float*>(smem + a.off_xs);  // {X, f} per (group of a unit, token)
-  float* red = reinterpret_cast<float*>(smem + a.off_red);  // [max_slabs][16 warps][16 rows][Mp]
+  // parked sums: [max_slabs][16 warps][16 rows][Mp], or (compact) [16 warps][2][16 rows][Mp]
+  float* red = reinterpret_cast<float*>(smem + a.off_red);
   const uint32_t full = sbase + (uint32_t)a.off_ctl;      // [16 warps][NS] mbarriers
   int* flags = reinterpret_cast<int*>(smem + a.off_ctl + 8 * kSW * NS);  // [0] a wait ran out, [1] bad header
 
@@ -382,8 +375,11 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
     flags[1] = 0;
     mbar_init_fence();
   }
-  // parked sums start at zero: a warp writes only the slabs its run touches
-  for (int i = threadIdx.x; i < nslabs * kSW * 16 * Mp; i += kSThreads) red[i] = 0.f;
+  // Parked sums start at zero: a warp writes only the slabs its run touches.
+  // Compact form: a warp's run touches at most two slabs (it is shorter than
+  // a slab: a CTA never holds more than 16 slabs), so each warp has two
+  // slots, for the slab of its first unit and the next.
+  for (int i = threadIdx.x; i < (a.compact ? 2 * kSW : nslabs * kSW) * 16 * Mp; i += kSThreads) red[i] = 0.f;
   __syncthreads();
   // The static weights start streaming before the previous kernel on the
   // stream has finished; x, y and the workspace wait for it.
@@ -474,7 +470,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   int cur = g0 / KT;  // slab of the running sums
   // park this warp's sums of slab `cur` and go on with the next slab
   auto flush = [&]() {
-    float* rb = red + (size_t)((cur - s0) * kSW + warp) * 16 * Mp;
+    float* rb = red + (size_t)(a.compact ? warp * 2 + (cur - g0 / KT) : (cur - s0) * kSW + warp) * 16 * Mp;
     if (ONE) {
       if (t == 0) {
         rb[gr] = yacc[0];
@@ -514,8 +510,12 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
         xu[j] = xres + (kt + j) * x_unit + o.x;
         xsu[j] = xsum + ((kt + j) * GPT * xs_row + (ONE ? 0 : 2 * t)) * 2;
       }
+      if (S % 2 == 0) {  // two units at a time: four independent accumulator chains
 #pragma unroll
-      for (int j = 0; j < S; j += 2) units_step<BITS, GPT, ONE, 2>(W + j, xu + j, xsu + j, xs_half, yacc);
+        for (int j = 0; j < S; j += 2) units_step<BITS, GPT, ONE, 2>(W + j, xu + j, xsu + j, xs_half, yacc);
+      } else {
+        units_step<BITS, GPT, ONE, S>(W, xu, xsu, xs_half, yacc);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < S; ++j) {
@@ -560,7 +560,22 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
     const int sl = q / per, idx = q - sl * per;
     const int row = ONE ? idx : idx / Mp, tok = ONE ? 0 : idx - row * Mp;
     const int nn = (s0 + sl) * kSlabN + row;
-    if (tok < a.M && nn < a.N) store_out(a, BITS, tok, nn, sum_warps(red + (size_t)sl * kSW * per + idx, per), row >= 8);
+    if (tok >= a.M || nn >= a.N) continue;
+    float v = 0.f;
+    if (!a.compact) {
+#pragma unroll
+      for (int w = 0; w < kSW; ++w) v += red[(size_t)(sl * kSW + w) * per + idx];
+    } else {
+      // the warps whose runs touch slab s0 + sl, in warp order
+#pragma unroll 4
+      for (int w = 0; w < kSW; ++w) {
+        int wg0, wnu;
+        warp_run(u0, u1, w, wg0, wnu);
+        const int d = s0 + sl - wg0 / KT;  // slot of this slab in warp w
+        if (wnu > 0 && (d == 0 || d == 1)) v += red[(size_t)(w * 2 + d) * per + idx];
+      }
+    }
+    store_out(a, BITS, tok, nn, v, row >= 8);
   }
 }
 
@@ -578,34 +593,43 @@ int stream_plan(const Geometry& G, int M, StreamPlan* P) {
   StreamPlan S{};
   S.G = sms;
   S.Mp = M == 1 ? 1 : (M + 1) / 2 * 2;
-  const int stage = warp_stage_units(G.bits) * G.unit_bytes;
   S.max_slabs = (nslab + S.G - 1) / S.G;
   const int xres = (G.KT * M * 256 + 127) / 128 * 128;
   const int xs = (G.KT * G.gpt * (M == 1 ? 1 : 8) * 8 + 127) / 128 * 128;
-  const int red = S.max_slabs * kSW * 16 * S.Mp * 4;
-  for (int ns = TF_STREAM_NS_MAX; ns >= 2; --ns) {
-    const int ring = (kSW * ns * stage + 127) / 128 * 128;
-    const int ctl = 8 * kSW * ns + 8;
-    const size_t smem = 128 + (size_t)ring + xres + xs + red + ctl;
-    if (smem <= (size_t)kSmemMax) {
-      S.NS = ns;
-      S.npre = TF_STREAM_NPRE < ns ? TF_STREAM_NPRE : ns;
-      S.off_x = ring;
-      S.off_xs = S.off_x + xres;
-      S.off_red = S.off_xs + xs;
-      S.off_ctl = S.off_red + red;
-      S.smem = smem;
-      *P = S;
-      return 1;
+  // full-size stages and one parked slot per (slab, warp) first; then
+  // half-size stages; then two parked slots per warp
+  for (int cfg = 0; cfg < 4; ++cfg) {
+    const int half = cfg & 1, compact = cfg >> 1;
+    if (compact && S.max_slabs > kSW) break;  // two slots need runs shorter than a slab
+    const int red = (compact ? 2 : S.max_slabs) * kSW * 16 * S.Mp * 4;
+    const int stage = warp_stage_units(G.bits, half != 0) * G.unit_bytes;
+    for (int ns = TF_STREAM_NS_MAX; ns >= 2; --ns) {
+      const int ring = (kSW * ns * stage + 127) / 128 * 128;
+      const int ctl = 8 * kSW * ns + 8;
+      const size_t smem = 128 + (size_t)ring + xres + xs + red + ctl;
+      if (smem <= (size_t)kSmemMax) {
+        S.half = half;
+        S.compact = compact;
+        S.NS = ns;
+        S.npre = TF_STREAM_NPRE < ns ? TF_STREAM_NPRE : ns;
+        S.off_x = ring;
+        S.off_xs = S.off_x + xres;
+        S.off_red = S.off_xs + xs;
+        S.off_ctl = S.off_red + red;
+        S.smem = smem;
+        *P = S;
+        return 1;
+      }
     }
   }
   return 0;
 }
 
 template <int BITS, int GPT, bool ONE>
-static int launch_stream(const StreamArgs& a, size_t smem, cudaStream_t s) {
-  static std::atomic<unsigned long long> opted{0};
-  return launch_pdl(gemv_stream_kernel<BITS, GPT, ONE>, opted, a.G, kSThreads, kSmemMax, smem, s, a);
+static int launch_stream(const StreamArgs& a, bool half, size_t smem, cudaStream_t s) {
+  static std::atomic<unsigned long long> opted{0}, opted_half{0};
+  if (half) return launch_pdl(gemv_stream_kernel<BITS, GPT, ONE, true>, opted_half, a.G, kSThreads, kSmemMax, smem, s, a);
+  return launch_pdl(gemv_stream_kernel<BITS, GPT, ONE, false>, opted, a.G, kSThreads, kSmemMax, smem, s, a);
 }
 
 int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
@@ -620,13 +644,16 @@ int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const u
   a.NS = P.NS; a.npre = P.npre;
   a.off_x = P.off_x; a.off_xs = P.off_xs; a.off_red = P.off_red; a.off_ctl = P.off_ctl;
   a.max_slabs = P.max_slabs;
-  const bool one = M == 1;
+  a.compact = P.compact;
+  const bool one = M == 1, h = P.half != 0;
   if (G.bits == 4) {
-    if (G.gpt == 1) return one ? launch_stream<4, 1, true>(a, P.smem, stream) : launch_stream<4, 1, false>(a, P.smem, stream);
-    return one ? launch_stream<4, 2, true>(a, P.smem, stream) : launch_stream<4, 2, false>(a, P.smem, stream);
+    if (G.gpt == 1)
+      return one ? launch_stream<4, 1, true>(a, h, P.smem, stream) : launch_stream<4, 1, false>(a, h, P.smem, stream);
+    return one ? launch_stream<4, 2, true>(a, h, P.smem, stream) : launch_stream<4, 2, false>(a, h, P.smem, stream);
   }
-  if (G.gpt == 1) return one ? launch_stream<8, 1, true>(a, P.smem, stream) : launch_stream<8, 1, false>(a, P.smem, stream);
-  return one ? launch_stream<8, 2, true>(a, P.smem, stream) : launch_stream<8, 2, false>(a, P.smem, stream);
+  if (G.gpt == 1)
+    return one ? launch_stream<8, 1, true>(a, h, P.smem, stream) : launch_stream<8, 1, false>(a, h, P.smem, stream);
+  return one ? launch_stream<8, 2, true>(a, h, P.smem, stream) : launch_stream<8, 2, false>(a, h, P.smem, stream);
 }
 
 }  // namespace tf

@@ -36,7 +36,7 @@ int encode_units_map(const uint8_t* units, int S, int KT, int unit_bytes, CUtens
 // SM, groups of 64, any multiple of 128 or per channel; no workspace.
 // stream_plan returns 1 and fills *P when it takes the layer.
 struct StreamPlan {
-  int G, Mp, NS, npre, off_x, off_xs, off_red, off_ctl, max_slabs;
+  int G, Mp, NS, npre, off_x, off_xs, off_red, off_ctl, max_slabs, half, compact;
   size_t smem;
 };
 int stream_plan(const Geometry& G, int M, StreamPlan* P);

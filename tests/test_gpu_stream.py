@@ -45,6 +45,7 @@ STREAM_FORMATS = [
     (2440, 1016, 4, 0), (2440, 1152, 4, 128), (2432, 4096, 4, 64), (3000, 2048, 8, 0),
     (2560, 1280, 8, 64), (5000, 3072, 4, 128), (2450, 384, 4, 128), (2448, 1024, 4, 256),
     (2447, 520, 4, 0), (2500, 640, 8, 128), (2433, 136, 8, 0), (4104, 8192, 4, 128),
+    (2600, 8192, 8, 0), (2440, 8192, 4, 64),  # M = 8: activations of 128 KB, half-size ring stages
 ]
 
 
