@@ -23,7 +23,7 @@ import numpy as np
 __all__ = [
     "TFError", "lib", "lib_path", "version", "prepack_size", "prepack", "prepack_awq", "unprepack",
     "blob_info", "Weights", "dequant", "gemv", "gemv_workspace_size", "gemv_noalloc", "gemm",
-    "gemm_workspace_size", "device_error",
+    "gemm_workspace_size", "device_error", "test_stall_copies",
     "header_declarations",
 ]
 
@@ -65,6 +65,7 @@ _SIGNATURES = {
     "tf_gemm_bias": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
     "tf_gemv_noalloc": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
     "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
+    "tf_test_stall_copies": (_i, [_i, ctypes.c_uint]),
 }
 
 
@@ -351,3 +352,8 @@ def device_error() -> int:
     v = ctypes.c_uint()
     _check(_lib().tf_device_error(ctypes.byref(v)), "tf_device_error")
     return v.value
+
+
+def test_stall_copies(stall: bool, timeout_us: int = 0) -> None:
+    """Failure-detection test hook (see tf_test_stall_copies in include/tf.h)."""
+    _check(_lib().tf_test_stall_copies(1 if stall else 0, timeout_us), "tf_test_stall_copies")

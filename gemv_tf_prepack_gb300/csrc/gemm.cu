@@ -46,7 +46,6 @@ constexpr int kEpilogueWarp0 = 2;    // warps 2..5
 constexpr int kEpilogueThreads = 128;
 constexpr int kSlabBytesW = 128 * 128;  // 128 rows x 64 BF16
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
-constexpr uint64_t kTimeoutNs = 4000000000ull;
 // Epilogue staging: two buffers of 16 tokens x 128 rows of BF16 (one TMA box each).
 constexpr int kEpiChunk = 16;
 constexpr int kEpiStageBytes = 2 * kEpiChunk * kTileN * 2;
@@ -71,6 +70,8 @@ struct GemmArgs {
   int dp_tiles;               // tiles [0, dp_tiles) whole per CTA; the rest split along K
   int sk_ctas;                // CTAs [0, sk_ctas) share the split tiles' k-iterations (at least one each)
   int P, OPS;                 // stages of the packed ring and of the operand ring
+  uint64_t wait_ns;           // limit of every wait
+  int stall;                  // failure-detection test: the producers issue no copies
   int y_tma;                  // 1: whole tiles leave through shared-memory staging and TMA stores
   int off_op, off_epi, off_bar;  // byte offsets in the 1024-aligned dynamic smem
 };
@@ -211,14 +212,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       while (ok && sched_next(a, sc, wk)) {
         const int nb = wk.tile / a.MT;
         for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
-          ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, kTimeoutNs);
+          ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, a.wait_ns);
           if (!ok) break;
-          mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
           const uint32_t dst = sbase + (uint32_t)(ps * a.tile_bytes);
-          if (BITS == 4)
-            tma_load_3d(dst, &tmw, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
-          else
-            tma_load_4d(dst, &tmw, 0, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
+          if (!a.stall) {
+            mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
+            if (BITS == 4)
+              tma_load_3d(dst, &tmw, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
+            else
+              tma_load_4d(dst, &tmw, 0, 0, kt, nb * kSlabsPerTile, B.full_p + 8 * ps);
+          }
           if (++ps == a.P) { ps = 0; pph ^= 1; }
         }
       }
@@ -238,11 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int mt = wk.tile % a.MT;
         for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
           for (int h = 0; h < 2; ++h) {
-            ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, kTimeoutNs);
+            ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrProducerWait, a.wait_ns);
             if (!ok) break;
-            mbar_arrive_expect_tx(B.full_op + 8 * os, x_slab_bytes);
-            tma_load_2d(sbase + a.off_op + (uint32_t)os * op_stage_bytes + kSlabBytesW, &tmx,
-                        kt * kTileK + h * 64, mt * a.BN, B.full_op + 8 * os);
+            if (!a.stall) {
+              mbar_arrive_expect_tx(B.full_op + 8 * os, x_slab_bytes);
+              tma_load_2d(sbase + a.off_op + (uint32_t)os * op_stage_bytes + kSlabBytesW, &tmx,
+                          kt * kTileK + h * 64, mt * a.BN, B.full_op + 8 * os);
+            }
             if (++os == a.OPS) { os = 0; oph ^= 1; }
           }
         }
@@ -259,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       Sched sc = sched_begin(a);
       Work wk;
       while (ok && sched_next(a, sc, wk)) {
-        ok = mbar_wait(B.tempty + 8 * acc, aph ^ 1, err, kErrMmaWait, kTimeoutNs);
+        ok = mbar_wait(B.tempty + 8 * acc, aph ^ 1, err, kErrMmaWait, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * 256;
         const int nslabs = 2 * (wk.ke - wk.kb);
         for (int sl = 0; sl < nslabs; ++sl) {
-          ok = mbar_wait(B.full_op + 8 * os, oph, err, kErrMmaWait, kTimeoutNs);
+          ok = mbar_wait(B.full_op + 8 * os, oph, err, kErrMmaWait, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t wsl = sbase + a.off_op + (uint32_t)os * op_stage_bytes;
@@ -285,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (issued) {
         // wait for every MMA of this CTA before tensor memory is released
         umma_commit(B.drain);
-        mbar_wait(B.drain, 0, err, kErrDrain, kTimeoutNs);
+        mbar_wait(B.drain, 0, err, kErrDrain, a.wait_ns);
       }
     }
   } else if (warp >= kEpilogueWarp0 && warp < kDequantWarp0) {
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     Work wk;
     while (ok && sched_next(a, sc, wk)) {
       const int nb = wk.tile / a.MT, mt = wk.tile - nb * a.MT;
-      ok = mbar_wait(B.tfull + 8 * acc, aph, err, kErrEpilogueWait, kTimeoutNs);
+      ok = mbar_wait(B.tfull + 8 * acc, aph, err, kErrEpilogueWait, a.wait_ns);
       // the four epilogue warps meet at named barriers below: they must all
       // go on, or all stop
       ok = named_barrier_and(kEpilogueThreads, ok);
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     Work wk;
     while (ok && sched_next(a, sc, wk)) {
       for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
-        ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, kTimeoutNs);
+        ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, a.wait_ns);
         if (!ok) break;
         const uint8_t* pk = smem + (size_t)ps * a.tile_bytes;
         const uint32_t sp = *reinterpret_cast<const uint32_t*>(pk + s_off);
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         const unsigned os = slab % (unsigned)a.OPS;
         const uint32_t oph = (slab / (unsigned)a.OPS) & 1u;
-        ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, kTimeoutNs);
+        ok = mbar_wait(B.empty_op + 8 * os, oph ^ 1, err, kErrDequantWait, a.wait_ns);
         if (!ok) break;
         uint8_t* wsl = smem + a.off_op + (size_t)os * op_stage_bytes;
         *reinterpret_cast<uint4*>(wsl + dst[0][0]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -677,6 +682,9 @@ int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
   P.a.bias = bias;
   P.a.err = device_error_ptr();
   if (!P.a.err) return TF_ERR_CUDA;
+  const TestHook hook = test_hook();
+  P.a.wait_ns = hook.wait_ns;
+  P.a.stall = hook.stall;
   CUtensorMap map, wmap, ymap;
   rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
   if (rc) return rc;

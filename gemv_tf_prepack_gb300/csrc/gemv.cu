@@ -103,7 +103,6 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = 32 * kGemvWarps;
-constexpr uint64_t kGemvTimeoutNs = 4000000000ull;
 constexpr uint64_t kGemvDrainNs = 200000000ull;  // bounded wait for copies still in flight after an error
 constexpr unsigned kErrGemvWait = 0x600;
 
@@ -220,8 +219,8 @@ __device__ __forceinline__ uint8_t* align128(uint8_t* p) {
 
 // Wait on a ring barrier with every lane; the result is the same for the
 // whole warp (a lane that gave up makes the warp give up).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* err) {
-  return mbar_wait_warp(bar, parity, err, kErrGemvWait, kGemvTimeoutNs);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* err, uint64_t wait_ns) {
+  return mbar_wait_warp(bar, parity, err, kErrGemvWait, wait_ns);
 }
 
 // ===========================================================================
@@ -258,6 +257,8 @@ struct GemvArgs {
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
   unsigned* err;
   long long T;
+  uint64_t wait_ns;  // limit of every wait
+  int stall;         // failure-detection test: issue no copies
   int N, K, M, KT, g, G, S_max, group;
   int NS, stage_bytes, x_off;  // shared-memory ring: stages, bytes per stage, x slice offset
 };
@@ -359,6 +360,7 @@ __device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap*
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
   const int i = f * TPS;
   const int n = ntile - i < TPS ? ntile - i : TPS;
+  if (a.stall) return;
   const uint32_t x_bytes = (uint32_t)a.M * 256u;
   const uint32_t bar = full + 8u * s;
   const uint32_t dst = sbase + (uint32_t)(s * a.stage_bytes);
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   int s = 0;
   uint32_t lap = 0;
   for (int f = 0; f < nfill; ++f) {
-    if (!warp_wait(full + 8 * s, lap & 1u, a.err)) break;
+    if (!warp_wait(full + 8 * s, lap & 1u, a.err, a.wait_ns)) break;
     const int i0 = f * kTilesPerStage;
     const int n = ntile - i0 < kTilesPerStage ? ntile - i0 : kTilesPerStage;
     const uint8_t* st = smem + s * a.stage_bytes;
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
             mbar_arrive(empty + 8 * s);
             if (atomicAdd(released + s, 1u) == kGemvWarps - 1) {
               released[s] = 0;
-              refill = f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, kGemvTimeoutNs);
+              refill = f + a.NS < nfill && mbar_wait(empty + 8 * s, lap & 1u, a.err, kErrGemvWait, a.wait_ns);
             }
           }
           if (__shfl_sync(0xFFFFFFFFu, refill, 0))
@@ -531,6 +533,8 @@ struct SlabArgs {
   uint16_t* y;
   const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
   unsigned* err;
+  uint64_t wait_ns;  // limit of every wait
+  int stall;         // failure-detection test: issue no copies
   int N, K, M, KT, g, group;
   int nslab, spc, QPS;  // slabs holding real rows, slabs per CTA, ring fills per slab
   int NS, stage_bytes, xres_off, red_off, ctl_off;  // offsets in the 128-aligned shared memory
@@ -563,7 +567,7 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
   const int n = a.KT - k0 < U ? a.KT - k0 : U;
   const uint32_t bar = full + 8u * st;
   const uint32_t dst = sbase + (uint32_t)(st * a.stage_bytes);
-  if (lane == 0) {
+  if (lane == 0 && !a.stall) {
     mbar_arrive_expect_tx(bar, (uint32_t)(n * UB));
     bulk_load(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar);
   }
@@ -580,7 +584,7 @@ __device__ __forceinline__ void hand_back_stage(const SlabArgs& a, uint32_t sbas
   if (lane == 0 && atom_add_acq_rel_cta(released + st, 1u) == NW - 1) {
     released[st] = 0;
     refill = !dead && f + a.NS < nfill;
-    if (refill) atomicAdd(ctl, 1);
+    if (refill && !a.stall) atomicAdd(ctl, 1);
   }
   if (__shfl_sync(0xFFFFFFFFu, refill, 0)) slab_fill<BITS, GPT, NW>(a, sbase, full, s0, f + a.NS, st, lane);
 }
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
       mbar_init(full + 8 * i, 1);
       released[i] = 0;
     }
-    ctl[0] = npre;
+    ctl[0] = a.stall ? 0 : npre;  // fills issued
     ctl[1] = 0;
     mbar_init_fence();
   }
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
   for (int f = 0; f < nfill; ++f) {
     const bool whole = q < a.QPS - 1 || last_n == U;  // every warp has UPW units in this stage
     const int n = whole ? U : last_n;
-    if (!dead && !warp_wait(full + 8 * st, lap & 1u, a.err)) dead = true;
+    if (!dead && !warp_wait(full + 8 * st, lap & 1u, a.err, a.wait_ns)) dead = true;
     const uint8_t* xp = xq;
     if (!dead) {
 #pragma unroll
@@ -859,10 +863,12 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
              uint16_t* y, int M, float4* partials, unsigned* counters, cudaStream_t stream) {
   unsigned* err = device_error_ptr();
   if (!err) return TF_ERR_CUDA;
+  const TestHook hook = test_hook();
   const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   if (P.slab) {
     SlabArgs a;
     a.units = units; a.x = x; a.y = y; a.bias = bias; a.err = err;
+    a.wait_ns = hook.wait_ns; a.stall = hook.stall;
     a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
     a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS;
     a.NS = P.NS; a.stage_bytes = P.stage_bytes; a.xres_off = P.xres_off;
@@ -881,6 +887,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
   if (rc) return rc;
   GemvArgs a;
   a.units = units; a.y = y; a.bias = bias; a.partials = partials; a.counters = counters; a.err = err;
+  a.wait_ns = hook.wait_ns; a.stall = hook.stall;
   a.T = P.T;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
   a.G = P.G; a.S_max = P.S_max;

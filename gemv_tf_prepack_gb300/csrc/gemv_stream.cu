@@ -67,7 +67,6 @@ namespace {
 constexpr int kSW = TF_STREAM_WARPS;  // warps per CTA
 constexpr int kSThreads = 32 * kSW;
 constexpr int kSmemMax = 227 * 1024;  // one CTA per SM
-constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr unsigned kErrStreamWait = 0x700;
 
@@ -87,6 +86,8 @@ struct StreamArgs {
   int off_x, off_xs, off_red, off_ctl;  // byte offsets in the 128-aligned dynamic shared memory
   int max_slabs;         // slabs of the busiest CTA
   int compact;           // parked sums: 1 = two slots per warp, 0 = one slot per (slab, warp)
+  int stall;             // failure-detection test: issue no copies, so that the first wait runs out
+  uint64_t wait_ns;      // limit of every wait
 };
 
 // The run of units of warp w of a CTA whose units are [u0, u1).
@@ -101,6 +102,7 @@ __device__ __forceinline__ void warp_run(int u0, int u1, int w, int& g0, int& nu
 template <int BITS, int GPT>
 __device__ __forceinline__ void warp_fill(const StreamArgs& a, uint32_t dst, uint32_t bar, int g, int n) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
+  if (a.stall) return;
   mbar_arrive_expect_tx_relaxed(bar, (uint32_t)(n * UB));
   bulk_load(dst, a.units + (size_t)g * UB, (uint32_t)(n * UB), bar);
 }
@@ -456,8 +458,8 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   if (dead && threadIdx.x == 0) atomicCAS(a.err, 0u, kErrBlobHeader);
   // x is in: the rest of the rings follows (requested earlier, these stages
   // would have reached the SM ahead of the activations)
-  int issued = npre;  // stages of this warp requested so far
-  if (!dead) {
+  int issued = a.stall ? 0 : npre;  // stages of this warp requested so far
+  if (!dead && !a.stall) {
     if (lane == 0)
       for (int i = npre; i < nring; ++i)
         warp_fill<BITS, GPT>(a, ring + (uint32_t)(i * SB), wbar + 8u * i, g0 + i * S, nu - i * S < S ? nu - i * S : S);
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
     const int lo = g0 + i * S, n = nu - i * S < S ? nu - i * S : S;  // units [lo, lo + n)
     // one lane waits (suspended in hardware between polls), the warp follows
     unsigned ok = 1;
-    if (lane == 0) ok = mbar_wait_sleep(wbar + 8u * slot, par, a.err, kErrStreamWait, kWaitNs) ? 1u : 0u;
+    if (lane == 0) ok = mbar_wait_sleep(wbar + 8u * slot, par, a.err, kErrStreamWait, a.wait_ns) ? 1u : 0u;
     if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
       dead = true;
       break;
@@ -645,6 +647,9 @@ int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const u
   a.off_x = P.off_x; a.off_xs = P.off_xs; a.off_red = P.off_red; a.off_ctl = P.off_ctl;
   a.max_slabs = P.max_slabs;
   a.compact = P.compact;
+  const TestHook hook = test_hook();
+  a.stall = hook.stall;
+  a.wait_ns = hook.wait_ns;
   const bool one = M == 1, h = P.half != 0;
   if (G.bits == 4) {
     if (G.gpt == 1)

@@ -29,7 +29,24 @@ unsigned* device_error_ptr() {
   return static_cast<unsigned*>(p);
 }
 
+namespace {
+std::atomic<int> g_stall{0};
+std::atomic<unsigned long long> g_wait_ns{0};
+}  // namespace
+
+TestHook test_hook() {
+  const unsigned long long w = g_wait_ns.load(std::memory_order_acquire);
+  return TestHook{g_stall.load(std::memory_order_acquire), w ? (uint64_t)w : 4000000000ull};
+}
+
 }  // namespace tf
+
+extern "C" int tf_test_stall_copies(int stall, unsigned int timeout_us) {
+  if (stall && timeout_us == 0) return TF_ERR_INVALID_ARG;
+  tf::g_wait_ns.store(stall ? (unsigned long long)timeout_us * 1000ull : 0ull, std::memory_order_release);
+  tf::g_stall.store(stall ? 1 : 0, std::memory_order_release);
+  return TF_OK;
+}
 
 extern "C" int tf_device_error(unsigned int* code) {
   if (!code) return TF_ERR_INVALID_ARG;

@@ -15,6 +15,15 @@ namespace tf {
 // Device address of the current device's error word (cached per device).
 unsigned* device_error_ptr();
 
+// The failure-detection test hook (tf_test_stall_copies): while `stall` is
+// set, kernels issue no weight or activation copies, and every bounded wait
+// gives up after wait_ns (4 s when the hook is off).
+struct TestHook {
+  int stall;
+  uint64_t wait_ns;
+};
+TestHook test_hook();
+
 // TMA maps over the activations x [M, K] (BF16, row-major); columns past K
 // and rows past M read as zero.  encode_x_map: box of 128 columns x M rows,
 // no swizzle (one GEMV tile's slice).  encode_x_map_sw128: box of 64

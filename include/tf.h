@@ -253,6 +253,19 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
                     const uint16_t* x, uint16_t* y, int M, cudaStream_t stream);
 
 /*
+ * Failure-detection test hook (the paper has no counterpart; off by
+ * default, process-wide, not for production use).  While stall is nonzero,
+ * every later device call issues no weight or activation copies, so its
+ * first bounded wait runs out after timeout_us microseconds (> 0): the
+ * kernel records its wait code in the device error word (see
+ * tf_device_error), writes no output and exits with no copy in flight, and
+ * the device stays usable.  tf_test_stall_copies(0, 0) turns it off and
+ * restores the 4-second limit.  TF_ERR_INVALID_ARG for stall with
+ * timeout_us == 0.
+ */
+int tf_test_stall_copies(int stall, unsigned int timeout_us);
+
+/*
  * Read and clear the current device's error word (synchronous).  Kernels
  * that wait on on-chip barriers give up after a bounded time instead of
  * hanging, set a nonzero code here and exit; *code receives 0 if nothing
