@@ -64,6 +64,11 @@ _SIGNATURES = {
     "tf_gemm": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
     "tf_gemm_bias": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
     "tf_gemv_noalloc": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _i, _p]),
+    "tf_prepack_gate_up": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _sz]),
+    "tf_gemv_silu_gate": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
+    "tf_gemm_silu_gate": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _i, _p, _sz, _p]),
+    "tf_gemv_qkv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
+    "tf_gemm_qkv": (_i, [_p, _sz, _i, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
     "tf_device_error": (_i, [ctypes.POINTER(ctypes.c_uint)]),
     "tf_test_stall_copies": (_i, [_i, ctypes.c_uint]),
 }
@@ -128,6 +133,32 @@ def prepack(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, N: int, 
     out = np.empty(prepack_size(N, K, bits, group), dtype=np.uint8)
     _check(_lib().tf_prepack(qw.ctypes.data, s.ctypes.data, z.ctypes.data, N, K, bits, group,
                              out.ctypes.data, out.size), "tf_prepack")
+    return out
+
+
+def _natural(qweight, scales, zeros, N: int, K: int, bits: int, group: int):
+    qw = np.ascontiguousarray(qweight, dtype=np.uint32 if bits == 4 else np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    z = np.ascontiguousarray(zeros, dtype=np.uint8)
+    g = K if group == 0 else group
+    want_qw = (N, K // 8) if bits == 4 else (N, K)
+    if qw.shape != want_qw or s.shape != (N, K // g) or z.shape != (N, K // g):
+        raise ValueError("qweight/scales/zeros shapes do not match N, K, bits, group")
+    return qw, s, z
+
+
+def prepack_gate_up(gate, up, F: int, K: int, bits: int, group: int) -> np.ndarray:
+    """One blob of N = 2F rows from the gate and up projections of a gated MLP.
+
+    gate and up are (qweight, scales, zeros) in natural order, each F x K;
+    rows are interleaved in blocks of 8 (``tf_prepack_gate_up`` in include/tf.h).
+    """
+    gq, gs, gz = _natural(*gate, F, K, bits, group)
+    uq, us, uz = _natural(*up, F, K, bits, group)
+    out = np.empty(prepack_size(2 * F, K, bits, group), dtype=np.uint8)
+    _check(_lib().tf_prepack_gate_up(gq.ctypes.data, gs.ctypes.data, gz.ctypes.data, uq.ctypes.data,
+                                     us.ctypes.data, uz.ctypes.data, F, K, bits, group, out.ctypes.data,
+                                     out.size), "tf_prepack_gate_up")
     return out
 
 
@@ -345,6 +376,89 @@ def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True, bias
         _check(_lib().tf_gemm_bias(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(),
                                    bias.data_ptr(), y.data_ptr(), M, wp, wn, _stream_handle(stream)), "tf_gemm_bias")
     return y
+
+
+def _bf16_out(t, shape, name: str):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor {list(shape)}")
+    return t
+
+
+def _epi_call(W: Weights, x, kind: str, workspace, stream, stream_k: bool):
+    _check_x(W, x)
+    M = x.shape[0]
+    if kind == "gemm" and not stream_k:
+        return M, None, 0
+    wp, wn = _workspace_args(W, M, kind, workspace)
+    return M, wp, wn
+
+
+def _silu_gate(W: Weights, x, h, bias, workspace, stream, kind: str, stream_k: bool):
+    """h[M, N/2] = silu(gate) * up of a layer packed by prepack_gate_up.
+
+    kind "gemv" (1 <= M <= 8) calls tf_gemv_silu_gate, "gemm" (any M)
+    tf_gemm_silu_gate; bias is in the layer's (interleaved) row order.
+    """
+    torch = _torch()
+    if kind not in ("gemv", "gemm"):
+        raise ValueError("kind must be 'gemv' or 'gemm'")
+    M, wp, wn = _epi_call(W, x, kind, workspace, stream, stream_k)
+    shape = (M, W.N // 2)
+    h = torch.empty(shape, dtype=torch.bfloat16, device=W.blob.device) if h is None else _bf16_out(h, shape, "h")
+    if bias is not None:
+        _check_bias(W, bias)
+    fn = "tf_gemv_silu_gate" if kind == "gemv" else "tf_gemm_silu_gate"
+    _check(getattr(_lib(), fn)(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(),
+                               None if bias is None else bias.data_ptr(), h.data_ptr(), M, wp, wn,
+                               _stream_handle(stream)), fn)
+    return h
+
+
+def _qkv(W: Weights, x, nq: int, nk: int, out, bias, workspace, stream, kind: str, stream_k: bool):
+    """(q [M, nq], k [M, nk], v [M, N - nq - nk]) of a stacked QKV layer, written by the epilogue.
+
+    kind "gemv" (1 <= M <= 8) calls tf_gemv_qkv, "gemm" (any M) tf_gemm_qkv;
+    out, when given, is the (q, k, v) triple to write.
+    """
+    torch = _torch()
+    if kind not in ("gemv", "gemm"):
+        raise ValueError("kind must be 'gemv' or 'gemm'")
+    M, wp, wn = _epi_call(W, x, kind, workspace, stream, stream_k)
+    nv = W.N - nq - nk
+    shapes = ((M, nq), (M, nk), (M, nv))
+    if out is None:
+        out = tuple(torch.empty(sh, dtype=torch.bfloat16, device=W.blob.device) for sh in shapes)
+    else:
+        out = tuple(_bf16_out(t, sh, nm) for t, sh, nm in zip(out, shapes, ("q", "k", "v")))
+    if bias is not None:
+        _check_bias(W, bias)
+    ptrs = [t.data_ptr() if t.numel() else None for t in out]
+    fn = "tf_gemv_qkv" if kind == "gemv" else "tf_gemm_qkv"
+    _check(getattr(_lib(), fn)(W._blob_ptr, W._blob_bytes, W.N, W.K, W.bits, W.group, x.data_ptr(),
+                               None if bias is None else bias.data_ptr(), ptrs[0], ptrs[1], ptrs[2], nq, nk, M,
+                               wp, wn, _stream_handle(stream)), fn)
+    return out
+
+
+def gemv_silu_gate(W: Weights, x, h=None, bias=None, workspace=None, stream=None):
+    """tf_gemv_silu_gate: h[M, N/2] = silu(gate) * up for 1 <= M <= 8."""
+    return _silu_gate(W, x, h, bias, workspace, stream, "gemv", True)
+
+
+def gemm_silu_gate(W: Weights, x, h=None, bias=None, workspace=None, stream=None, stream_k=True):
+    """tf_gemm_silu_gate: h[M, N/2] = silu(gate) * up for any M."""
+    return _silu_gate(W, x, h, bias, workspace, stream, "gemm", stream_k)
+
+
+def gemv_qkv(W: Weights, x, nq: int, nk: int, out=None, bias=None, workspace=None, stream=None):
+    """tf_gemv_qkv: (q, k, v) of a stacked QKV layer for 1 <= M <= 8."""
+    return _qkv(W, x, nq, nk, out, bias, workspace, stream, "gemv", True)
+
+
+def gemm_qkv(W: Weights, x, nq: int, nk: int, out=None, bias=None, workspace=None, stream=None, stream_k=True):
+    """tf_gemm_qkv: (q, k, v) of a stacked QKV layer for any M."""
+    return _qkv(W, x, nq, nk, out, bias, workspace, stream, "gemm", stream_k)
 
 
 def device_error() -> int:

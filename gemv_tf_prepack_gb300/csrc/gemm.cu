@@ -60,8 +60,7 @@ enum : unsigned {
 
 struct GemmArgs {
   const uint8_t* units;
-  uint16_t* y;
-  const uint16_t* bias;       // BF16 [N] added before the final rounding, or null
+  Epi epi;                    // where y goes (plain, SiLU gate or split) and the bias
   unsigned* err;              // device error word
   float* ws;                  // stream-K partial sums: [CTA][2][BN / 16][128 rows][16]
   unsigned* cnt;              // stream-K arrivals per tile (zero on entry and on exit)
@@ -72,9 +71,21 @@ struct GemmArgs {
   int P, OPS;                 // stages of the packed ring and of the operand ring
   uint64_t wait_ns;           // limit of every wait
   int stall;                  // failure-detection test: the producers issue no copies
-  int y_tma;                  // 1: whole tiles leave through shared-memory staging and TMA stores
+  int y_tma;                  // 1: whole tiles of a plain y leave through shared-memory staging and TMA stores
   int off_op, off_epi, off_bar;  // byte offsets in the 1024-aligned dynamic smem
 };
+
+// Token m's biased sum v of this thread's row n, through the epilogue.  All
+// 32 lanes of the warp (32 consecutive rows from a multiple of 32) call it
+// together: the SiLU gate takes the up row's sum from lane + 8.
+__device__ __forceinline__ void put_y(const Epi& e, int m, int n, float v) {
+  if (e.mode == kEpiSiluGate) {
+    const float u = __shfl_down_sync(0xFFFFFFFFu, v, 8);
+    if ((n & 8) == 0 && n < e.N) epi_put_gate(e, m, n, v, u);
+  } else if (n < e.N) {
+    epi_put(e, m, n, v);
+  }
+}
 
 struct Bars {
   uint32_t full_p, empty_p, full_op, empty_op, tfull, tempty, drain, tmem_slot, flag;
@@ -324,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (!ok) break;
       tc_fence_after();
       const int n = nb * kTileN + row;
-      const bool has_bias = a.bias != nullptr;
-      const float bv = has_bias && n < a.N ? bf16_bits_to_float(a.bias[n]) : 0.f;
+      const bool has_bias = a.epi.bias != nullptr;
+      const float bv = has_bias && n < a.N ? bf16_bits_to_float(a.epi.bias[n]) : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256;
       const bool whole = wk.kb == 0 && wk.ke == a.KT;
       const int ti = wk.tile - a.dp_tiles;
@@ -358,15 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
         } else if (whole) {
           const int m0 = mt * a.BN + c0;
-          if (n < a.N) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int m = m0 + j;
-              if (m < a.M)
-                a.y[(size_t)m * a.N + n] = __bfloat16_as_ushort(
-                    __float2bfloat16_rn(has_bias ? __uint_as_float(r[j]) + bv : __uint_as_float(r[j])));
-            }
-          }
+          for (int j = 0; j < 16; ++j)
+            if (m0 + j < a.M) put_y(a.epi, m0 + j, n, has_bias ? __uint_as_float(r[j]) + bv : __uint_as_float(r[j]));
         } else {
           float4* dst = reinterpret_cast<float4*>(mine + ((size_t)(c0 / 16) * 128 + row) * 16);
 #pragma unroll
@@ -414,17 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               v[j].x += u[j].x; v[j].y += u[j].y; v[j].z += u[j].z; v[j].w += u[j].w;
             }
           }
-          if (n < a.N) {
-            const int m0 = mt * a.BN + c0;
+          const int m0 = mt * a.BN + c0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+          for (int j = 0; j < 4; ++j) {
+            const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (m0 + 4 * j + e < a.M)
-                  a.y[(size_t)(m0 + 4 * j + e) * a.N + n] =
-                      __bfloat16_as_ushort(__float2bfloat16_rn(has_bias ? vv[e] + bv : vv[e]));
-            }
+            for (int e = 0; e < 4; ++e)
+              if (m0 + 4 * j + e < a.M) put_y(a.epi, m0 + 4 * j + e, n, has_bias ? vv[e] + bv : vv[e]);
           }
         }
         if (row == 0) a.cnt[ti] = 0u;
@@ -551,7 +552,7 @@ struct GemmPlan {
 
 // stream_k: split the tiles of the last, partial wave (plus one whole wave)
 // along K; needs the workspace sized by ws_bytes + cnt_bytes.
-int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
+int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P) {
   GemmArgs& a = P->a;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
   a.tile_bytes = kSlabsPerTile * G.unit_bytes;
@@ -559,8 +560,8 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, GemmPlan* P) {
   a.MT = (M + a.BN - 1) / a.BN;
   a.ntiles = G.NB * a.MT;
   const int op_stage = kSlabBytesW + a.BN * 128;
-  // y as a TMA tensor needs rows of a multiple of 16 bytes
-  a.y_tma = G.N % 8 == 0 ? 1 : 0;
+  // y as a TMA tensor needs rows of a multiple of 16 bytes (and a plain y)
+  a.y_tma = G.N % 8 == 0 && epi_mode == kEpiPlain ? 1 : 0;
   const int epi = a.y_tma ? kEpiStageBytes : 0;
   a.OPS = 0;
   for (int ops = 4; ops >= 2 && a.OPS == 0; --ops)
@@ -637,6 +638,50 @@ int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorM
   return launch_status();
 }
 
+// The GEMM of one call, y written through epi.
+int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+             const Epi& epi, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Geometry G;
+  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
+  if (rc) return rc;
+  if (!x || M < 1) return TF_ERR_INVALID_ARG;
+  rc = check_epi(epi);
+  if (rc) return rc;
+  if (!aligned16(x) || !aligned16(workspace) || (epi.mode == kEpiPlain && !aligned16(epi.y))) return TF_ERR_ALIGNMENT;
+  GemmPlan P;
+  rc = gemm_plan(G, M, workspace != nullptr, epi.mode, &P);
+  if (rc) return rc;
+  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes) return TF_ERR_WORKSPACE;
+  P.a.ws = static_cast<float*>(workspace);
+  P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
+  P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
+  P.a.epi = epi;
+  P.a.err = device_error_ptr();
+  if (!P.a.err) return TF_ERR_CUDA;
+  const TestHook hook = test_hook();
+  P.a.wait_ns = hook.wait_ns;
+  P.a.stall = hook.stall;
+  CUtensorMap map, wmap, ymap;
+  rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
+  if (rc) return rc;
+  rc = encode_units_map(P.a.units, G.S, G.KT, G.unit_bytes, &wmap);
+  if (rc) return rc;
+  if (P.a.y_tma) {
+    rc = encode_y_map(epi.y, M, N, &ymap);
+    if (rc) return rc;
+  } else {
+    memset(&ymap, 0, sizeof(ymap));  // not read by the kernel
+  }
+  if (bits == 4) {
+    if (G.gpt == 1) return launch_gemm<4, 1>(map, wmap, ymap, P, stream);
+    if (G.gpt == 2) return launch_gemm<4, 2>(map, wmap, ymap, P, stream);
+    return launch_gemm<4, 4>(map, wmap, ymap, P, stream);
+  }
+  if (G.gpt == 1) return launch_gemm<8, 1>(map, wmap, ymap, P, stream);
+  if (G.gpt == 2) return launch_gemm<8, 2>(map, wmap, ymap, P, stream);
+  return launch_gemm<8, 4>(map, wmap, ymap, P, stream);
+}
+
 }  // namespace
 }  // namespace tf
 
@@ -651,7 +696,7 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
   if (rc) return rc;
   if (M < 1) return TF_ERR_INVALID_ARG;
   GemmPlan P;
-  rc = gemm_plan(G, M, true, &P);
+  rc = gemm_plan(G, M, true, kEpiPlain, &P);
   if (rc) return rc;
   *bytes = P.ws_bytes + P.cnt_bytes;
   return TF_OK;
@@ -665,45 +710,22 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
 int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
                  const uint16_t* bias, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream) {
-  Geometry G;
-  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
-  if (rc) return rc;
-  if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(bias) & 1))
-    return TF_ERR_ALIGNMENT;
-  GemmPlan P;
-  rc = gemm_plan(G, M, workspace != nullptr, &P);
-  if (rc) return rc;
-  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes) return TF_ERR_WORKSPACE;
-  P.a.ws = static_cast<float*>(workspace);
-  P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
-  P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
-  P.a.y = y;
-  P.a.bias = bias;
-  P.a.err = device_error_ptr();
-  if (!P.a.err) return TF_ERR_CUDA;
-  const TestHook hook = test_hook();
-  P.a.wait_ns = hook.wait_ns;
-  P.a.stall = hook.stall;
-  CUtensorMap map, wmap, ymap;
-  rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
-  if (rc) return rc;
-  rc = encode_units_map(P.a.units, G.S, G.KT, G.unit_bytes, &wmap);
-  if (rc) return rc;
-  if (P.a.y_tma) {
-    rc = encode_y_map(y, M, N, &ymap);
-    if (rc) return rc;
-  } else {
-    memset(&ymap, 0, sizeof(ymap));  // not read by the kernel
-  }
-  if (bits == 4) {
-    if (G.gpt == 1) return launch_gemm<4, 1>(map, wmap, ymap, P, stream);
-    if (G.gpt == 2) return launch_gemm<4, 2>(map, wmap, ymap, P, stream);
-    return launch_gemm<4, 4>(map, wmap, ymap, P, stream);
-  }
-  if (G.gpt == 1) return launch_gemm<8, 1>(map, wmap, ymap, P, stream);
-  if (G.gpt == 2) return launch_gemm<8, 2>(map, wmap, ymap, P, stream);
-  return launch_gemm<8, 4>(map, wmap, ymap, P, stream);
+  Epi e{y, nullptr, nullptr, bias, kEpiPlain, N, M, 0, 0};
+  return gemm_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemm_silu_gate(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                      const uint16_t* bias, uint16_t* h, int M, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  Epi e{h, nullptr, nullptr, bias, kEpiSiluGate, N, M, 0, 0};
+  return gemm_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemm_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                const uint16_t* bias, uint16_t* q, uint16_t* k, uint16_t* v, int nq, int nk, int M, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+  Epi e{q, k, v, bias, kEpiSplit3, N, M, nq, nk};
+  return gemm_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

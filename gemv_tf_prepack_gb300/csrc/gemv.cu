@@ -196,20 +196,22 @@ __device__ __forceinline__ void mma_unit(const WRegs<BITS, GPT>& R, const uint32
   mma_half(R, 1, xs[1], acc[1]);
 }
 
-// v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1; bias
-// (BF16 [N], or null) is added to each sum before its one rounding to BF16.
-__device__ __forceinline__ void store_y(uint16_t* y, const uint16_t* bias, int N, int M, int n0, int t,
-                                        const float (&v)[4]) {
+// v = this lane's sums for rows n0, n0 + 8 and tokens 2t, 2t + 1, written
+// through the epilogue (which adds the bias before the one rounding to BF16).
+// In the SiLU-gate epilogue n0 is a gate row and n0 + 8 its up row.
+__device__ __forceinline__ void store_y(const Epi& e, int n0, int t, const float (&v)[4]) {
   const int m0 = 2 * t, m1 = 2 * t + 1, n1 = n0 + 8;
-  if (n0 < N) {
-    const float b = bias ? bf16_bits_to_float(bias[n0]) : 0.f;
-    if (m0 < M) y[(size_t)m0 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[0] + b : v[0]));
-    if (m1 < M) y[(size_t)m1 * N + n0] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[1] + b : v[1]));
+  if (n0 >= e.N) return;
+  if (e.mode == kEpiSiluGate) {
+    if (m0 < e.M) epi_put_gate(e, m0, n0, epi_biased(e, n0, v[0]), epi_biased(e, n1, v[2]));
+    if (m1 < e.M) epi_put_gate(e, m1, n0, epi_biased(e, n0, v[1]), epi_biased(e, n1, v[3]));
+    return;
   }
-  if (n1 < N) {
-    const float b = bias ? bf16_bits_to_float(bias[n1]) : 0.f;
-    if (m0 < M) y[(size_t)m0 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[2] + b : v[2]));
-    if (m1 < M) y[(size_t)m1 * N + n1] = __bfloat16_as_ushort(__float2bfloat16_rn(bias ? v[3] + b : v[3]));
+  if (m0 < e.M) epi_put(e, m0, n0, epi_biased(e, n0, v[0]));
+  if (m1 < e.M) epi_put(e, m1, n0, epi_biased(e, n0, v[1]));
+  if (n1 < e.N) {
+    if (m0 < e.M) epi_put(e, m0, n1, epi_biased(e, n1, v[2]));
+    if (m1 < e.M) epi_put(e, m1, n1, epi_biased(e, n1, v[3]));
   }
 }
 
@@ -251,8 +253,7 @@ static_assert(tiles_per_stage(4) * kSlabsPerTile <= 32 && tiles_per_stage(8) * k
 
 struct GemvArgs {
   const uint8_t* units;
-  uint16_t* y;
-  const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
+  Epi epi;  // where y goes (plain, SiLU gate or split) and the bias
   float4* partials;    // [G][S_max][8 warps][32 lanes]
   unsigned* counters;  // [NB][8 warps], zero on entry and on exit
   unsigned* err;
@@ -280,7 +281,7 @@ __device__ __forceinline__ bool end_segment(const GemvArgs& a, int c, long long 
                                             int lane, const float (&v)[4]) {
   const int gr = lane >> 2, t = lane & 3;
   if (whole) {
-    store_y(a.y, a.bias, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, v);
+    store_y(a.epi, nb * kTileN + warp * kSlabN + gr, t, v);
     return false;
   }
   const int seg = nb - (int)(t0 / a.KT);
@@ -320,7 +321,7 @@ __device__ __forceinline__ void publish_segment(const GemvArgs& a, int nb, int w
       }
     }
   }
-  store_y(a.y, a.bias, a.N, a.M, nb * kTileN + warp * kSlabN + gr, t, s);
+  store_y(a.epi, nb * kTileN + warp * kSlabN + gr, t, s);
   if (lane == 0) a.counters[nb * 8 + warp] = 0u;
 }
 
@@ -530,8 +531,7 @@ __host__ __device__ constexpr int slab_units_per_warp(int bits, int nw) {
 struct SlabArgs {
   const uint8_t* units;
   const uint16_t* x;
-  uint16_t* y;
-  const uint16_t* bias;  // BF16 [N] added before the final rounding, or null
+  Epi epi;  // where y goes (plain, SiLU gate or split) and the bias
   unsigned* err;
   uint64_t wait_ns;  // limit of every wait
   int stall;         // failure-detection test: issue no copies
@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) gemv_slab_kernel(con
           v[0] += u.x; v[1] += u.y; v[2] += u.z; v[3] += u.w;
         }
       }
-      store_y(a.y, a.bias, a.N, a.M, (s0 + i) * kSlabN + gr, t, v);
+      store_y(a.epi, (s0 + i) * kSlabN + gr, t, v);
     }
   }
   if (threadIdx.x == 0 && ctl[1]) {
@@ -859,15 +859,15 @@ int launch_slab(const SlabArgs& a, int nw, int grid, size_t smem, cudaStream_t s
 
 // The GEMV of a checked layer with a plan; partials / counters are the
 // tile GEMV's scratch (unused by the slab GEMV).
-int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
-             uint16_t* y, int M, float4* partials, unsigned* counters, cudaStream_t stream) {
+int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint16_t* x, const Epi& epi, int M,
+             float4* partials, unsigned* counters, cudaStream_t stream) {
   unsigned* err = device_error_ptr();
   if (!err) return TF_ERR_CUDA;
   const TestHook hook = test_hook();
   const uint8_t* units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   if (P.slab) {
     SlabArgs a;
-    a.units = units; a.x = x; a.y = y; a.bias = bias; a.err = err;
+    a.units = units; a.x = x; a.epi = epi; a.err = err;
     a.wait_ns = hook.wait_ns; a.stall = hook.stall;
     a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
     a.nslab = P.nslab; a.spc = P.spc; a.QPS = P.QPS;
@@ -886,7 +886,7 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
   int rc = encode_x_map(x, M, G.K, &map);
   if (rc) return rc;
   GemvArgs a;
-  a.units = units; a.y = y; a.bias = bias; a.partials = partials; a.counters = counters; a.err = err;
+  a.units = units; a.epi = epi; a.partials = partials; a.counters = counters; a.err = err;
   a.wait_ns = hook.wait_ns; a.stall = hook.stall;
   a.T = P.T;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
@@ -905,6 +905,29 @@ int run_gemv(const Geometry& G, const GemvPlan& P, const void* blob, const uint1
 template <int BITS, int GPT>
 void launch_dequant(const uint8_t* units, const Geometry& G, unsigned* err, uint16_t* w, cudaStream_t s) {
   dequant_kernel<BITS, GPT><<<G.NB * G.KT, 512, 0, s>>>(units, G.N, G.K, G.KT, G.g, G.group, err, w);
+}
+
+// The GEMV of one call, y written through epi.
+int gemv_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+             const Epi& epi, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Geometry G;
+  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
+  if (rc) return rc;
+  if (!x || M < 1) return TF_ERR_INVALID_ARG;
+  if (M > 8) return TF_ERR_UNSUPPORTED;
+  rc = check_epi(epi);
+  if (rc) return rc;
+  if (!aligned16(x) || !aligned16(workspace)) return TF_ERR_ALIGNMENT;
+  StreamPlan SP;
+  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, epi, M, stream);
+  GemvPlan P;
+  rc = gemv_plan(G, M, &P);
+  if (rc) return rc;
+  const size_t need = gemv_scratch_bytes(P);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
+  return run_gemv(G, P, blob, x, epi, M, static_cast<float4*>(workspace),
+                  need ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes) : nullptr,
+                  stream);
 }
 
 }  // namespace
@@ -963,22 +986,22 @@ int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
 int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
                  const uint16_t* bias, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream) {
-  Geometry G;
-  int rc = check_blob(blob, blob_bytes, N, K, bits, group, &G);
-  if (rc) return rc;
-  if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
-  if (M > 8) return TF_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(bias) & 1)) return TF_ERR_ALIGNMENT;
-  StreamPlan SP;
-  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, bias, y, M, stream);
-  GemvPlan P;
-  rc = gemv_plan(G, M, &P);
-  if (rc) return rc;
-  const size_t need = gemv_scratch_bytes(P);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
-  return run_gemv(G, P, blob, x, bias, y, M, static_cast<float4*>(workspace),
-                  need ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes) : nullptr,
-                  stream);
+  Epi e{y, nullptr, nullptr, bias, kEpiPlain, N, M, 0, 0};
+  return gemv_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemv_silu_gate(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                      const uint16_t* bias, uint16_t* h, int M, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  Epi e{h, nullptr, nullptr, bias, kEpiSiluGate, N, M, 0, 0};
+  return gemv_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
+}
+
+int tf_gemv_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
+                const uint16_t* bias, uint16_t* q, uint16_t* k, uint16_t* v, int nq, int nk, int M, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+  Epi e{q, k, v, bias, kEpiSplit3, N, M, nq, nk};
+  return gemv_epi(blob, blob_bytes, N, K, bits, group, x, e, M, workspace, workspace_bytes, stream);
 }
 
 // ===========================================================================
@@ -1026,20 +1049,21 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
   if (!x || !y || M < 1) return TF_ERR_INVALID_ARG;
   if (M > 8) return TF_ERR_UNSUPPORTED;
   if (!aligned16(x)) return TF_ERR_ALIGNMENT;
+  const Epi e{y, nullptr, nullptr, nullptr, kEpiPlain, N, M, 0, 0};
   StreamPlan SP;
-  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, nullptr, y, M, stream);
+  if (stream_plan(G, M, &SP)) return run_stream(G, SP, blob, x, e, M, stream);
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
   if (gemv_scratch_bytes(P) > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
-  if (P.slab) return run_gemv(G, P, blob, x, nullptr, y, M, nullptr, nullptr, stream);
+  if (P.slab) return run_gemv(G, P, blob, x, e, M, nullptr, nullptr, stream);
   unsigned char* scratch = gemv_scratch_address();
   if (!scratch) return TF_ERR_CUDA;
   // The arrival counters must start at zero; a call cut short (device error)
   // could have left them dirty, so clear them on the stream first.
   unsigned char* counters = scratch + P.partial_bytes;
   if (cudaMemsetAsync(counters, 0, P.counter_bytes, stream) != cudaSuccess) return TF_ERR_CUDA;
-  return run_gemv(G, P, blob, x, nullptr, y, M, reinterpret_cast<float4*>(scratch),
+  return run_gemv(G, P, blob, x, e, M, reinterpret_cast<float4*>(scratch),
                   reinterpret_cast<unsigned*>(counters), stream);
 }
 

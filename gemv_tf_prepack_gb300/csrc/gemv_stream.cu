@@ -77,8 +77,7 @@ __host__ __device__ constexpr int warp_stage_units(int bits, bool half) { return
 struct StreamArgs {
   const uint8_t* units;  // the blob's units (after the header)
   const uint16_t* x;     // [M, K] BF16
-  uint16_t* y;           // [M, N] BF16
-  const uint16_t* bias;  // [N] BF16, or null
+  Epi epi;               // where y goes (plain, SiLU gate or split) and the bias
   unsigned* err;
   int nslab;             // slabs holding real rows
   int N, K, M, Mp, KT, G, group;
@@ -318,13 +317,6 @@ __device__ __forceinline__ uint32_t h2_bits(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // slab reductions
 
-// y[tok][nn] = bf16_rne(v (/ 16 for the INT4 rows gr + 8, whose codes carry
-// 16 q) + bias[nn]).
-__device__ __forceinline__ void store_out(const StreamArgs& a, int bits, int tok, int nn, float v, bool hi) {
-  float out = bits == 4 && hi ? v * 0.0625f : v;
-  if (a.bias) out += bf16_bits_to_float(a.bias[nn]);
-  a.y[(size_t)tok * a.N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(out));
-}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -557,12 +549,9 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   if (flags[0] || flags[1]) return;
 
   // Add the sixteen warps' parked sums of every slab in warp order; write y.
+  // (The INT4 rows gr + 8 carry 16 q: their sums are divided by 16 here.)
   const int per = 16 * Mp;
-  for (int q = threadIdx.x; q < nslabs * per; q += kSThreads) {
-    const int sl = q / per, idx = q - sl * per;
-    const int row = ONE ? idx : idx / Mp, tok = ONE ? 0 : idx - row * Mp;
-    const int nn = (s0 + sl) * kSlabN + row;
-    if (tok >= a.M || nn >= a.N) continue;
+  auto parked = [&](int sl, int idx) {
     float v = 0.f;
     if (!a.compact) {
 #pragma unroll
@@ -577,7 +566,21 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
         if (wnu > 0 && (d == 0 || d == 1)) v += red[(size_t)(w * 2 + d) * per + idx];
       }
     }
-    store_out(a, BITS, tok, nn, v, row >= 8);
+    return v;
+  };
+  const bool gate = a.epi.mode == kEpiSiluGate;
+  for (int q = threadIdx.x; q < nslabs * per; q += kSThreads) {
+    const int sl = q / per, idx = q - sl * per;
+    const int row = ONE ? idx : idx / Mp, tok = ONE ? 0 : idx - row * Mp;
+    const int nn = (s0 + sl) * kSlabN + row;
+    if (tok >= a.M || nn >= a.N || (gate && row >= 8)) continue;
+    const float v = parked(sl, idx);
+    if (gate) {  // gate row nn (row < 8) with its up row nn + 8
+      const float u = parked(sl, idx + 8 * Mp);
+      epi_put_gate(a.epi, tok, nn, epi_biased(a.epi, nn, v), epi_biased(a.epi, nn + 8, BITS == 4 ? u * 0.0625f : u));
+    } else {
+      epi_put(a.epi, tok, nn, epi_biased(a.epi, nn, BITS == 4 && row >= 8 ? v * 0.0625f : v));
+    }
   }
 }
 
@@ -634,11 +637,11 @@ static int launch_stream(const StreamArgs& a, bool half, size_t smem, cudaStream
   return launch_pdl(gemv_stream_kernel<BITS, GPT, ONE, false>, opted, a.G, kSThreads, kSmemMax, smem, s, a);
 }
 
-int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
-               uint16_t* y, int M, cudaStream_t stream) {
+int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const Epi& epi, int M,
+               cudaStream_t stream) {
   StreamArgs a;
   a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
-  a.x = x; a.y = y; a.bias = bias;
+  a.x = x; a.epi = epi;
   a.err = device_error_ptr();
   if (!a.err) return TF_ERR_CUDA;
   a.nslab = (G.N + kSlabN - 1) / kSlabN;

@@ -250,6 +250,36 @@ int tf_prepack_awq(const int32_t* qweight, const int32_t* qzeros, const uint16_t
   return TF_OK;
 }
 
+int tf_prepack_gate_up(const void* gate_qweight, const uint16_t* gate_scales, const uint8_t* gate_zeros,
+                       const void* up_qweight, const uint16_t* up_scales, const uint8_t* up_zeros, int F, int K,
+                       int bits, int group, void* out, size_t out_bytes) {
+  if (!gate_qweight || !gate_scales || !gate_zeros || !up_qweight || !up_scales || !up_zeros || !out)
+    return TF_ERR_INVALID_ARG;
+  if (F < 8 || F % 8 != 0 || F > 16384) return TF_ERR_INVALID_ARG;
+  const int N = 2 * F;
+  Geometry G;
+  int rc = tf::make_geometry(N, K, bits, group, &G);
+  if (rc) return rc;
+  if (out_bytes < G.total_bytes) return TF_ERR_INVALID_ARG;
+  // Interleave the rows in blocks of 8 (gate, up, gate, up, ...) into one
+  // natural-order layer and pack that.
+  const int n_groups = K / G.g;
+  const size_t row_bytes = bits == 4 ? (size_t)K / 2 : (size_t)K;
+  std::vector<uint8_t> q((size_t)N * row_bytes);
+  std::vector<uint16_t> s((size_t)N * n_groups);
+  std::vector<uint8_t> z((size_t)N * n_groups);
+  for (int r = 0; r < N; ++r) {
+    const bool up = (r & 15) >= 8;
+    const int f = (r >> 4) * 8 + (r & 7);
+    const uint8_t* qs = static_cast<const uint8_t*>(up ? up_qweight : gate_qweight);
+    memcpy(&q[(size_t)r * row_bytes], qs + (size_t)f * row_bytes, row_bytes);
+    memcpy(&s[(size_t)r * n_groups], (up ? up_scales : gate_scales) + (size_t)f * n_groups,
+           n_groups * sizeof(uint16_t));
+    memcpy(&z[(size_t)r * n_groups], (up ? up_zeros : gate_zeros) + (size_t)f * n_groups, n_groups);
+  }
+  return tf_prepack(q.data(), s.data(), z.data(), N, K, bits, group, out, out_bytes);
+}
+
 int tf_blob_info(const void* header, size_t bytes, int* N, int* K, int* bits, int* group) {
   if (!header || bytes < (size_t)tf::kHeaderBytes) return TF_ERR_INVALID_ARG;
   tf::BlobHeader h;

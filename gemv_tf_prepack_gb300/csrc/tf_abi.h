@@ -41,6 +41,40 @@ int encode_y_map(const uint16_t* y, int M, int N, CUtensorMap* map);
 // {unit/16, 2, 1, 8}.
 int encode_units_map(const uint8_t* units, int S, int KT, int unit_bytes, CUtensorMap* map);
 
+// Output epilogues: fused steps after the product (the pages' kernels end
+// at the product).
+enum EpiMode : int {
+  kEpiPlain = 0,     // y[m, n]
+  kEpiSiluGate = 1,  // gate/up rows interleaved in blocks of 8: h[m, j] = silu(gate_j) * up_j
+  kEpiSplit3 = 2,    // rows [0, n1) -> y, [n1, n1 + n2) -> y1, the rest -> y2 (fused QKV)
+};
+
+// Where and how a kernel writes its FP32 sums.  The bias (BF16 [N], or
+// null) is added to each sum before anything else.
+struct Epi {
+  uint16_t* y;   // plain: [M, N]; silu gate: [M, N / 2]; split: [M, n1]
+  uint16_t* y1;  // split: [M, n2]
+  uint16_t* y2;  // split: [M, N - n1 - n2] (null when that is 0)
+  const uint16_t* bias;
+  int mode, N, M, n1, n2;
+};
+
+// Host checks of an epilogue (after the layer's): outputs present, 2-byte
+// aligned, and the mode's own rules (silu gate: N a multiple of 16; split:
+// n1 >= 1, n2 >= 0, n1 + n2 <= N).
+inline int check_epi(const Epi& e) {
+  auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
+  if (!e.y) return TF_ERR_INVALID_ARG;
+  if (odd(e.y) || odd(e.bias)) return TF_ERR_ALIGNMENT;
+  if (e.mode == kEpiSiluGate && e.N % 16 != 0) return TF_ERR_INVALID_ARG;
+  if (e.mode == kEpiSplit3) {
+    if (e.n1 < 1 || e.n2 < 0 || e.n1 > e.N - e.n2) return TF_ERR_INVALID_ARG;
+    if ((e.n2 > 0 && !e.y1) || (e.N - e.n1 - e.n2 > 0 && !e.y2)) return TF_ERR_INVALID_ARG;
+    if (odd(e.y1) || odd(e.y2)) return TF_ERR_ALIGNMENT;
+  }
+  return TF_OK;
+}
+
 // The stream GEMV (gemv_stream.cu): M <= 8, at least one 16-row slab per
 // SM, groups of 64, any multiple of 128 or per channel; no workspace.
 // stream_plan returns 1 and fills *P when it takes the layer.
@@ -49,8 +83,8 @@ struct StreamPlan {
   size_t smem;
 };
 int stream_plan(const Geometry& G, int M, StreamPlan* P);
-int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const uint16_t* bias,
-               uint16_t* y, int M, cudaStream_t stream);
+int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const Epi& epi, int M,
+               cudaStream_t stream);
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 

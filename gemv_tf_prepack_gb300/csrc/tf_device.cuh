@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "tf_abi.h"
 #include "tf_format.h"
 
 namespace tf {
@@ -114,6 +115,43 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// output epilogues (fused steps after the product; the pages' kernels end at
+// the product)
+
+// (EpiMode and Epi are declared with the host checks.)
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// v + bias[n] (v itself, -0 included, without a bias).
+__device__ __forceinline__ float epi_biased(const Epi& e, int n, float v) {
+  return e.bias ? v + bf16_bits_to_float(e.bias[n]) : v;
+}
+
+// Row n of token m with its biased sum v, rounded once to BF16 (plain or
+// split; the caller checks n < N and m < M).
+__device__ __forceinline__ void epi_put(const Epi& e, int m, int n, float v) {
+  const uint16_t b = to_bf16_bits(v);
+  if (e.mode != kEpiSplit3) {
+    e.y[(size_t)m * e.N + n] = b;
+  } else if (n < e.n1) {
+    e.y[(size_t)m * e.n1 + n] = b;
+  } else if (n < e.n1 + e.n2) {
+    e.y1[(size_t)m * e.n2 + (n - e.n1)] = b;
+  } else {
+    const int n3 = e.N - e.n1 - e.n2;
+    e.y2[(size_t)m * n3 + (n - e.n1 - e.n2)] = b;
+  }
+}
+
+// SiLU gate of gate row n (n mod 16 < 8, biased sum g) and its up row n + 8
+// (biased sum u): h[m, 8 (n / 16) + n mod 8] = bf16_rne(silu(g) * u) with
+// silu(a) = a / (1 + e^-a), all in FP32.
+__device__ __forceinline__ void epi_put_gate(const Epi& e, int m, int n, float g, float u) {
+  const float h = g / (1.f + __expf(-g)) * u;
+  e.y[(size_t)m * (e.N >> 1) + ((n >> 4) << 3) + (n & 7)] = to_bf16_bits(h);
 }
 
 // ---------------------------------------------------------------------------

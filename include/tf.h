@@ -49,8 +49,10 @@
 extern "C" {
 #endif
 
-#define TF_VERSION 4  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias; 4: tf_gemv_noalloc,
-                         TF_ERR_SCRATCH_LIMIT, device-side check of the blob header */
+#define TF_VERSION 5  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias; 4: tf_gemv_noalloc,
+                         TF_ERR_SCRATCH_LIMIT, device-side check of the blob header;
+                         5: tf_prepack_gate_up, tf_gemv_silu_gate, tf_gemm_silu_gate,
+                         tf_gemv_qkv, tf_gemm_qkv */
 
 #define TF_OK 0
 #define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */
@@ -120,6 +122,21 @@ int tf_prepack(const void* qweight, const uint16_t* scales, const uint8_t* zeros
  */
 int tf_prepack_awq(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales_f16,
                    int N, int K, int group, void* out, size_t out_bytes);
+
+/*
+ * Offline pre-tiling of the gate and up projections of a gated MLP into the
+ * one layer tf_gemv_silu_gate / tf_gemm_silu_gate take (host, synchronous,
+ * pure; an addition of this library, the pages fuse no epilogue).  Each
+ * projection is F x K in natural order (arrays as for tf_prepack, same bits
+ * and group); the blob is the layer of N = 2F rows whose rows 16j .. 16j + 7
+ * are gate rows 8j .. 8j + 7 and rows 16j + 8 .. 16j + 15 the up rows
+ * 8j .. 8j + 7 (its natural-order row r is gate row 8 (r / 16) + r mod 8
+ * when r mod 16 < 8, else that up row).  F must be a multiple of 8; out is
+ * a host buffer of at least tf_prepack_size(2F, K, bits, group) bytes.
+ */
+int tf_prepack_gate_up(const void* gate_qweight, const uint16_t* gate_scales, const uint8_t* gate_zeros,
+                       const void* up_qweight, const uint16_t* up_scales, const uint8_t* up_zeros,
+                       int F, int K, int bits, int group, void* out, size_t out_bytes);
 
 /*
  * Exact inverse of tf_prepack (host).  Reads N, K, bits, group from the
@@ -198,7 +215,9 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
  * to split the K dimension of its last, partial wave of output tiles across
  * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters.  0
  * when the tiles fill whole waves.  Like the GEMV workspace it must be
- * zero-filled before its first use, and every tf_gemm leaves it zero-filled.
+ * zero-filled before its first use, and every tf_gemm that completes leaves
+ * it zero-filled.  After a call that reported a device error
+ * (tf_device_error nonzero) zero it again before reusing it.
  */
 int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
@@ -226,6 +245,42 @@ int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int gro
 int tf_gemm_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
                  const uint16_t* x, const uint16_t* bias, uint16_t* y, int M, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Fused epilogues (additions of this library; the pages' kernels end at the
+ * product).  Each runs the GEMV or GEMM of the layer exactly as tf_gemv_bias
+ * / tf_gemm_bias do (same limits on M, same workspace, same sums) and
+ * changes only where the biased FP32 sums s[m, n] = sum_k x[m, k] w[n, k]
+ * (+ bias[n], bias in the layer's row order, or NULL) go.
+ *
+ * SiLU gate, for the gate/up projection of a gated MLP packed by
+ * tf_prepack_gate_up (N = 2F, a multiple of 16, else TF_ERR_INVALID_ARG):
+ *     h[m, 8j + i] = bf16_rne(silu(s[m, 16j + i]) * s[m, 16j + 8 + i]),
+ *     i = 0..7, silu(a) = a / (1 + e^-a), computed in FP32;
+ * h is device memory, BF16 [M, N/2], 2-byte aligned.  The N x M
+ * intermediate never reaches memory.
+ */
+int tf_gemv_silu_gate(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                      const uint16_t* x, const uint16_t* bias, uint16_t* h, int M, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+int tf_gemm_silu_gate(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                      const uint16_t* x, const uint16_t* bias, uint16_t* h, int M, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Split, for a fused QKV projection (the three weight matrices stacked
+ * along N into one layer): rows [0, nq) go to q [M, nq], rows
+ * [nq, nq + nk) to k [M, nk] and rows [nq + nk, N) to v [M, N - nq - nk],
+ * each BF16 row-major device memory, 2-byte aligned, rounded once as by
+ * tf_gemv_bias.  nq >= 1, nk >= 0, nq + nk <= N, else TF_ERR_INVALID_ARG; k
+ * (v) may be NULL only when it gets no rows.
+ */
+int tf_gemv_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                const uint16_t* x, const uint16_t* bias, uint16_t* q, uint16_t* k, uint16_t* v,
+                int nq, int nk, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int tf_gemm_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
+                const uint16_t* x, const uint16_t* bias, uint16_t* q, uint16_t* k, uint16_t* v,
+                int nq, int nk, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * tf_gemv without a caller-provided workspace, for callers that cannot

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol():
     lib = tf.lib()
     for d in decl:
         getattr(lib, d)
-    assert tf.version() == 4
+    assert tf.version() == 5
 
 
 @pytest.mark.parametrize("N,K,bits,group", [
@@ -137,6 +137,27 @@ def test_device_calls_validate_before_touching_the_gpu():
     assert lib.tf_gemm_bias(blob, size, 256, 512, 4, 128, x, None, None, 4, None, 0, None) == -1
     assert lib.tf_dequant(None, size, 256, 512, 4, 128, y, None) == -1
     assert lib.tf_dequant(blob, size, 256, 512, 4, 96, y, None) == -2
+    # the fused epilogues: the layer's checks, then the epilogue's own
+    for fn in (lib.tf_gemv_silu_gate, lib.tf_gemm_silu_gate):
+        assert fn(blob, size - 16, 256, 512, 4, 128, x, None, y, 1, None, 0, None) == -5
+        assert fn(blob, size, 256, 512, 4, 128, x, None, None, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, odd, y, 1, None, 0, None) == -3
+        assert fn(blob, size, 256, 512, 4, 128, x, None, ctypes.c_void_p(16385), 1, None, 0, None) == -3
+    size_n = tf.prepack_size(264, 512, 4, 128)  # N = 264: not a multiple of 16
+    assert lib.tf_gemv_silu_gate(blob, size_n, 264, 512, 4, 128, x, None, y, 1, None, 0, None) == -1
+    assert lib.tf_gemm_silu_gate(blob, size_n, 264, 512, 4, 128, x, None, y, 1, None, 0, None) == -1
+    assert lib.tf_gemv_silu_gate(blob, size, 256, 512, 4, 128, x, None, y, 9, None, 0, None) == -2
+    q, k, v = ctypes.c_void_p(16384), ctypes.c_void_p(24576), ctypes.c_void_p(32768)
+    for fn in (lib.tf_gemv_qkv, lib.tf_gemm_qkv):
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, k, v, 0, 64, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, k, v, 128, -1, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, k, v, 200, 57, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, None, v, 128, 64, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, k, None, 128, 64, 1, None, 0, None) == -1
+        assert fn(blob, size, 256, 512, 4, 128, x, None, q, k, ctypes.c_void_p(32769), 128, 64, 1, None, 0,
+                  None) == -3
+        assert fn(blob, size - 16, 256, 512, 4, 128, x, None, q, k, v, 128, 64, 1, None, 0, None) == -5
+    assert lib.tf_gemv_qkv(blob, size, 256, 512, 4, 128, x, None, q, k, v, 128, 64, 9, None, 0, None) == -2
 
 
 def test_header_serves_a_plain_c_client(tmp_path):
