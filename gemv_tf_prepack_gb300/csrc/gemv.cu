@@ -372,8 +372,8 @@ __device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap*
       const int j = lane / kSlabsPerTile, mb = lane % kSlabsPerTile;
       const long long tt = t0 + i + j;
       const int nb = (int)(tt / a.KT), kt = (int)(tt - (long long)nb * a.KT);
-      bulk_load(dst + (uint32_t)(lane * UB), a.units + ((size_t)(nb * kSlabsPerTile + mb) * a.KT + kt) * UB,
-                (uint32_t)UB, bar);
+      bulk_load_hint(dst + (uint32_t)(lane * UB), a.units + ((size_t)(nb * kSlabsPerTile + mb) * a.KT + kt) * UB,
+                     (uint32_t)UB, bar, l2_evict_first_policy());  // weights are read once per call
     }
   }
   if (x && lane == 0) {
@@ -569,7 +569,8 @@ __device__ __forceinline__ void slab_fill(const SlabArgs& a, uint32_t sbase, uin
   const uint32_t dst = sbase + (uint32_t)(st * a.stage_bytes);
   if (lane == 0 && !a.stall) {
     mbar_arrive_expect_tx(bar, (uint32_t)(n * UB));
-    bulk_load(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar);
+    bulk_load_hint(dst, a.units + ((size_t)sl * a.KT + k0) * UB, (uint32_t)(n * UB), bar,
+                   l2_evict_first_policy());  // weights are read once per call
   }
 }
 

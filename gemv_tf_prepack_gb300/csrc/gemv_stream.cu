@@ -103,7 +103,9 @@ __device__ __forceinline__ void warp_fill(const StreamArgs& a, uint32_t dst, uin
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
   if (a.stall) return;
   mbar_arrive_expect_tx_relaxed(bar, (uint32_t)(n * UB));
-  bulk_load(dst, a.units + (size_t)g * UB, (uint32_t)(n * UB), bar);
+  // the weights are read once per call: they should not push the
+  // activations and other live data out of L2
+  bulk_load_hint(dst, a.units + (size_t)g * UB, (uint32_t)(n * UB), bar, l2_evict_first_policy());
 }
 
 // ---------------------------------------------------------------------------
