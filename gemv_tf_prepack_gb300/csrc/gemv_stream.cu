@@ -29,7 +29,8 @@
 //    and zero in FP32".
 //
 // Work split.  Each CTA (one per SM) owns whole 16-row slabs, the slab count
-// shared out as evenly as whole slabs allow; a slab split between two CTAs
+// shared out as evenly as whole slabs allow (the CTAs that start first take
+// the extra ones); a slab split between two CTAs
 // would need a cross-SM reduction whose L2 round trip at the end of the
 // layer costs more than the up-to-one-slab imbalance.  The CTA's slabs are
 // one contiguous byte range of the blob (units are slab-major), shared out
@@ -289,16 +290,13 @@ __device__ __forceinline__ void units_step(const Unit<BITS, GPT>* W, const uint8
 // activations: BF16 [M, K] -> FP16 [kt][token][128] in shared memory, scaled
 // per token by a power of two, plus per-group sums
 
-// Largest BF16 exponent field of the eight values of a chunk.
-__device__ __forceinline__ uint32_t chunk_max_exponent(const uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t e = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = (w[i] >> 7) & 0xFFu, hi = (w[i] >> 23) & 0xFFu;
-    e = max(e, max(lo, hi));
-  }
-  return e;
+// The exponent fields of the eight BF16 values of a chunk, reduced to the
+// largest per 16-bit lane (two lanes per word, each holding its field << 7);
+// the sign and mantissa bits are masked off, so unsigned 16-bit maxima
+// order the fields.
+__device__ __forceinline__ uint32_t chunk_max_exponent2(const uint4 v) {
+  constexpr uint32_t kExp = 0x7F807F80u;
+  return __vmaxu2(__vmaxu2(v.x & kExp, v.y & kExp), __vmaxu2(v.z & kExp, v.w & kExp));
 }
 
 // Power-of-two exponent e that maps the largest |x| of a token (BF16
@@ -352,8 +350,14 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
 
   // This CTA's whole slabs [s0, s0 + nslabs), i.e. units [u0, u1), and this
   // warp's run [g0, g0 + nu) of them (memory order).
-  const int s0 = (int)((long long)c * a.nslab / a.G);
-  const int nslabs = (int)((long long)(c + 1) * a.nslab / a.G) - s0;
+  // The first nslab mod G CTAs take one slab more than the others.  Blocks
+  // are placed on SMs in index order as the previous kernel's blocks leave
+  // them, so the low indices start first: the extra slabs go where the
+  // stream starts earliest, and the last blocks to start have the least to
+  // do.
+  const int q_all = a.nslab / a.G, r_all = a.nslab - q_all * a.G;
+  const int s0 = c * q_all + (c < r_all ? c : r_all);
+  const int nslabs = q_all + (c < r_all ? 1 : 0);
   const int u0 = s0 * KT, u1 = (s0 + nslabs) * KT;
   int g0, nu;
   warp_run(u0, u1, warp, g0, nu);
@@ -411,9 +415,10 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
       for (int q = 0; q < kBatch; ++q) {
         const int b = base + q * 2 * kSW + hid;  // uniform over the half warp
         if (base + q * 2 * kSW >= nblk) break;   // uniform over the warp
-        uint32_t E = chunk_max_exponent(v[q]);
+        uint32_t E2 = chunk_max_exponent2(v[q]);
 #pragma unroll
-        for (int d = 1; d < 16; d <<= 1) E = max(E, __shfl_xor_sync(0xFFFFFFFFu, E, d));
+        for (int d = 1; d < 16; d <<= 1) E2 = __vmaxu2(E2, __shfl_xor_sync(0xFFFFFFFFu, E2, d));
+        const uint32_t E = max(E2 & 0xFFFFu, E2 >> 16) >> 7;  // largest exponent field of the block
         const int e = token_shift(E);
         const float sc = pow2f(e);
         const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
@@ -552,7 +557,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
 
   // Add the sixteen warps' parked sums of every slab in warp order; write y.
   // (The INT4 rows gr + 8 carry 16 q: their sums are divided by 16 here.)
-  const int per = 16 * Mp;
+  const int per = ONE ? 16 : 16 * Mp;
   auto parked = [&](int sl, int idx) {
     float v = 0.f;
     if (!a.compact) {
