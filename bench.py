@@ -74,9 +74,11 @@ def source_hash(files):
 
 
 GEMV_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemv_stream.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
-                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
+                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h",
+                "gemv_tf_prepack_gb300/csrc/tf_abi.h"]
 GEMM_SOURCES = ["gemv_tf_prepack_gb300/csrc/gemm.cu", "gemv_tf_prepack_gb300/csrc/tf_device.cuh",
-                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h"]
+                "gemv_tf_prepack_gb300/csrc/tf_sm100.cuh", "gemv_tf_prepack_gb300/csrc/tf_format.h",
+                "gemv_tf_prepack_gb300/csrc/tf_abi.h"]
 
 
 def recorded_traffic(kernel: str, sources):
