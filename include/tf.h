@@ -33,6 +33,11 @@
  *    TF_ERR_CUDA return means the launch itself failed.
  *  - Calls are thread-safe.  Two device calls that share a workspace must
  *    not run concurrently.
+ *  - Device state (the error word, the scratch array of tf_gemv_noalloc,
+ *    cached device attributes) is looked up once per device, in the context
+ *    current at the first call: the device's primary context, which the
+ *    CUDA runtime uses.  Calls under another driver context, or after
+ *    cudaDeviceReset while the library stays loaded, are not supported.
  *  - The host checks blob_bytes against (N, K, bits, group); the kernels also
  *    read the device blob's 64-byte header and, when it describes another
  *    layer (for instance a blob of the same size with N and K swapped), write

@@ -46,7 +46,7 @@ def _noalloc(W, x, y):
 
 
 @pytest.mark.parametrize("N,K,bits,group,M", [
-    (4096, 4096, 4, 128, 1),      # a decode projection (slab GEMV: no scratch needed)
+    (4096, 4096, 4, 128, 1),      # a decode projection (stream GEMV: no scratch needed)
     (1024, 11008, 4, 128, 1),     # few rows, long K: every row block is split over many CTAs
     (1000, 1016, 8, 0, 3),        # ragged N and K, INT8 per channel, several tokens
     (8192, 32768, 4, 128, 1),     # long K
@@ -65,3 +65,24 @@ def test_noalloc_matches_gemv_twice(N, K, bits, group, M):
         check_close(got, ref64, f"noalloc {N}x{K} w{bits} g{group} M={M}")
     # and against the oracle, as every other GEMV test does
     check_close(got, tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb), "noalloc vs oracle")
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", [(1024, 11008, 4, 128, 1), (4096, 4096, 4, 128, 1), (300, 256, 4, 32, 5)])
+def test_noalloc_allocates_nothing(N, K, bits, group, M):
+    """After a first call (which may load the kernel and look up the scratch
+    array's address), further calls leave the device's free memory and the
+    caching allocator's reservation exactly as they were."""
+    import torch
+    _, W = layer(N, K, bits, group, 43)
+    x = to_dev_bf16(synth.make_activations(M, K, 43))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    _noalloc(W, x, y)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    for _ in range(20):
+        _noalloc(W, x, y)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_reserved() == reserved0
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
