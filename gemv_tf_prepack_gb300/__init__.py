@@ -127,7 +127,7 @@ def prepack(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, N: int, 
     s = np.ascontiguousarray(scales, dtype=np.uint16)
     z = np.ascontiguousarray(zeros, dtype=np.uint8)
     g = K if group == 0 else group
-    want_qw = (N, K // 8) if bits == 4 else (N, K)
+    want_qw = (N, (K + 7) // 8) if bits == 4 else (N, K)
     if qw.shape != want_qw or s.shape != (N, K // g) or z.shape != (N, K // g):
         raise ValueError("qweight/scales/zeros shapes do not match N, K, bits, group")
     out = np.empty(prepack_size(N, K, bits, group), dtype=np.uint8)
@@ -141,7 +141,7 @@ def _natural(qweight, scales, zeros, N: int, K: int, bits: int, group: int):
     s = np.ascontiguousarray(scales, dtype=np.uint16)
     z = np.ascontiguousarray(zeros, dtype=np.uint8)
     g = K if group == 0 else group
-    want_qw = (N, K // 8) if bits == 4 else (N, K)
+    want_qw = (N, (K + 7) // 8) if bits == 4 else (N, K)
     if qw.shape != want_qw or s.shape != (N, K // g) or z.shape != (N, K // g):
         raise ValueError("qweight/scales/zeros shapes do not match N, K, bits, group")
     return qw, s, z
@@ -197,7 +197,7 @@ def unprepack(blob: np.ndarray):
     b = np.ascontiguousarray(blob, dtype=np.uint8)
     N, K, bits, group = blob_info(b)
     g = K if group == 0 else group
-    qw = np.zeros((N, K // 8), np.uint32) if bits == 4 else np.zeros((N, K), np.uint8)
+    qw = np.zeros((N, (K + 7) // 8), np.uint32) if bits == 4 else np.zeros((N, K), np.uint8)
     s = np.zeros((N, K // g), np.uint16)
     z = np.zeros((N, K // g), np.uint8)
     _check(_lib().tf_unprepack(b.ctypes.data, b.size, qw.ctypes.data, s.ctypes.data, z.ctypes.data),

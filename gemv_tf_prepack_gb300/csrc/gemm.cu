@@ -638,6 +638,26 @@ int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorM
   return launch_status();
 }
 
+// Bytes of the activations copied to rows of a multiple of 8 elements
+// (K % 8 != 0, per channel only: a TMA tensor's rows must be multiples of
+// 16 bytes), kept in the caller's workspace after the stream-K part.
+size_t padded_x_bytes(const Geometry& G, int M) {
+  if (G.K % 8 == 0) return 0;
+  const size_t k8 = (size_t)(G.K + 7) / 8 * 8;
+  return ((size_t)M * k8 * sizeof(uint16_t) + 255) / 256 * 256;
+}
+
+// xp[m, k] = x[m, k] for k < K, 0 for K <= k < K8.
+__global__ void __launch_bounds__(256) pad_x_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ xp, int M,
+                                                    int K, int K8) {
+  const size_t total = (size_t)M * K8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t m = i / K8;
+    const int k = (int)(i - m * K8);
+    xp[i] = k < K ? x[m * K + k] : (uint16_t)0;
+  }
+}
+
 // The GEMM of one call, y written through epi.
 int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
              const Epi& epi, int M, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -651,7 +671,9 @@ int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int gr
   GemmPlan P;
   rc = gemm_plan(G, M, workspace != nullptr, epi.mode, &P);
   if (rc) return rc;
-  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes) return TF_ERR_WORKSPACE;
+  const size_t pad_bytes = padded_x_bytes(G, M);
+  if (pad_bytes && !workspace) return TF_ERR_WORKSPACE;  // the padded activations live there
+  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes + pad_bytes) return TF_ERR_WORKSPACE;
   P.a.ws = static_cast<float*>(workspace);
   P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
   P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
@@ -662,7 +684,19 @@ int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int gr
   P.a.wait_ns = hook.wait_ns;
   P.a.stall = hook.stall;
   CUtensorMap map, wmap, ymap;
-  rc = encode_x_map_sw128(x, M, K, P.a.BN, &map);
+  const uint16_t* xa = x;
+  int ka = K;
+  if (pad_bytes) {
+    uint16_t* xp = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + P.ws_bytes + P.cnt_bytes);
+    ka = (K + 7) / 8 * 8;
+    const size_t total = (size_t)M * ka;
+    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    pad_x_kernel<<<blocks, 256, 0, stream>>>(x, xp, M, K, ka);
+    rc = launch_status();
+    if (rc) return rc;
+    xa = xp;
+  }
+  rc = encode_x_map_sw128(xa, M, ka, P.a.BN, &map);
   if (rc) return rc;
   rc = encode_units_map(P.a.units, G.S, G.KT, G.unit_bytes, &wmap);
   if (rc) return rc;
@@ -698,7 +732,7 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
   GemmPlan P;
   rc = gemm_plan(G, M, true, kEpiPlain, &P);
   if (rc) return rc;
-  *bytes = P.ws_bytes + P.cnt_bytes;
+  *bytes = P.ws_bytes + P.cnt_bytes + padded_x_bytes(G, M);
   return TF_OK;
 }
 

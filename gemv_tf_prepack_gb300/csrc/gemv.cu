@@ -93,8 +93,14 @@ __global__ void __launch_bounds__(512) dequant_kernel(const uint8_t* __restrict_
     if (n >= N) continue;
     const uint32_t* src = e ? hi : lo;
     uint16_t* dst = w + (size_t)n * K + k0;
-    if (k0 < K) *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
-    if (k0 + 8 < K) *reinterpret_cast<uint4*>(dst + 8) = make_uint4(src[4], src[5], src[6], src[7]);
+    if (K % 8 == 0) {  // rows of whole 16-byte pieces
+      if (k0 < K) *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
+      if (k0 + 8 < K) *reinterpret_cast<uint4*>(dst + 8) = make_uint4(src[4], src[5], src[6], src[7]);
+    } else {  // per channel with K % 8 != 0: element by element
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (k0 + c < K) dst[c] = (uint16_t)(src[c >> 1] >> (16 * (c & 1)));
+    }
   }
 }
 
@@ -798,6 +804,9 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   const int sms = sm_count();
   if (sms <= 0) return TF_ERR_CUDA;
   *P = GemvPlan{};
+  // these kernels move x rows as 16-byte pieces (the stream GEMV takes
+  // per-channel layers with K % 8 != 0 whenever their activations fit)
+  if (Gm.K % 8 != 0) return TF_ERR_UNSUPPORTED;
   const int nslab = (Gm.N + kSlabN - 1) / kSlabN;
   if (nslab >= sms && Gm.KT >= kGemvWarps) {
     // Enough slabs for every SM: whole slabs per CTA.

@@ -302,6 +302,19 @@ __device__ __forceinline__ uint32_t chunk_max_exponent2(const uint4 v) {
 // Power-of-two exponent e that maps the largest |x| of a token (BF16
 // exponent field E) below 2^15, clamped so that 2^e and 2^(24 - e) are normal
 // floats.
+// Eight BF16 activations from p, of which the first n (>= 1) exist (the
+// rest read as zero), element by element: rows of K % 8 != 0 values are
+// not 16-byte aligned.
+__device__ __forceinline__ uint4 load_x8(const uint16_t* p, int n) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = 2 * i < n ? __ldcg(p + 2 * i) : 0u, hi = 2 * i + 1 < n ? __ldcg(p + 2 * i + 1) : 0u;
+    w[i] = lo | hi << 16;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ int token_shift(uint32_t E) {
   const int e = 141 - (int)E;
   return e < -103 ? -103 : (e > 127 ? 127 : e);
@@ -409,7 +422,10 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
         const int kt = ONE ? b : b / a.M, m = ONE ? 0 : b - kt * a.M;
         const int col = kt * kTileK + 8 * r;
         v[q] = make_uint4(0, 0, 0, 0);
-        if (b < nblk && col < a.K) v[q] = __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + col));
+        if (b < nblk && col < a.K) {
+          const uint16_t* src = a.x + (size_t)m * a.K + col;
+          v[q] = a.K % 8 == 0 ? __ldcg(reinterpret_cast<const uint4*>(src)) : load_x8(src, a.K - col);
+        }
       }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
@@ -601,9 +617,12 @@ int stream_plan(const Geometry& G, int M, StreamPlan* P) {
   const int sms = sm_count();
   if (sms <= 0) return 0;
   const int nslab = (G.N + kSlabN - 1) / kSlabN;
-  if (nslab < sms) return 0;
+  // K % 8 != 0 (per channel only): the other GEMVs move x rows as 16-byte
+  // pieces, so this kernel takes every such layer, on fewer CTAs than SMs
+  // when the layer has fewer slabs
+  if (nslab < sms && G.K % 8 == 0) return 0;
   StreamPlan S{};
-  S.G = sms;
+  S.G = nslab < sms ? nslab : sms;
   S.Mp = M == 1 ? 1 : (M + 1) / 2 * 2;
   S.max_slabs = (nslab + S.G - 1) / S.G;
   const int xres = (G.KT * M * 256 + 127) / 128 * 128;

@@ -72,7 +72,7 @@ struct Source {
 
   int code(int n, int k) const {
     if (awq) return awq_nibble(awq->qweight[(size_t)k * (G.N / 8) + n / 8], n & 7);
-    if (G.bits == 4) return (q4[(size_t)n * (G.K / 8) + (k >> 3)] >> (4 * (k & 7))) & 0xF;
+    if (G.bits == 4) return (q4[(size_t)n * ((G.K + 7) / 8) + (k >> 3)] >> (4 * (k & 7))) & 0xF;
     return q8[(size_t)n * G.K + k];
   }
   // Group of padded column k (k may lie in the K padding of the last tile).
@@ -308,7 +308,7 @@ int tf_unprepack(const void* blob, size_t bytes, void* qweight, uint16_t* scales
   const uint8_t* b = (const uint8_t*)blob;
   const int n_groups = K / G.g;
   const int sb = tf::slot_bytes(bits);
-  if (bits == 4) std::memset(qweight, 0, (size_t)N * (K / 8) * 4);
+  if (bits == 4) std::memset(qweight, 0, (size_t)N * ((K + 7) / 8) * 4);
   // Slab s only holds rows s*16 .. s*16+15: no two slabs write the same word.
   parallel_slabs(G.S, [&](int s) {
     if (s * tf::kSlabN >= N) return;
@@ -327,7 +327,7 @@ int tf_unprepack(const void* blob, size_t bytes, void* qweight, uint16_t* scales
                 const uint32_t w = (uint32_t)slot[4 * j] | ((uint32_t)slot[4 * j + 1] << 8) |
                                    ((uint32_t)slot[4 * j + 2] << 16) | ((uint32_t)slot[4 * j + 3] << 24);
                 const int c = (w >> (4 * i)) & 0xF;
-                ((uint32_t*)qweight)[(size_t)n * (K / 8) + (k >> 3)] |= (uint32_t)c << (4 * (k & 7));
+                ((uint32_t*)qweight)[(size_t)n * ((K + 7) / 8) + (k >> 3)] |= (uint32_t)c << (4 * (k & 7));
               } else {
                 ((uint8_t*)qweight)[(size_t)n * K + k] = slot[8 * j + i];
               }

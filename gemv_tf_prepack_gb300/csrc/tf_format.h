@@ -90,7 +90,8 @@ inline int make_geometry(int N, int K, int bits, int group, Geometry* out) {
   if (N <= 0 || K <= 0) return -1;
   if (N > kMaxDim || K > kMaxDim) return -2;
   if (bits != 4 && bits != 8) return -2;
-  if (K % 8 != 0) return -1;
+  // K % 8 != 0 only per channel (every group size is a multiple of 8)
+  if (K % 8 != 0 && group != 0) return -1;
   if (group < 0) return -1;
   int g = group == 0 ? K : group;
   if (group != 0 && !(group == 32 || group == 64 || group % kTileK == 0)) return -2;

@@ -17,7 +17,8 @@ per-channel scales and zero points; W4A16 and W8A16, "Main contributions 1"):
   rounding half to even.  The scale is rounded to BF16 *before* z and q are
   derived from it.
 * INT4 codes are packed eight per uint32, low nibble first along K
-  (``qweight[n, c] = sum_j q[n, 8c + j] << 4j``); INT8 codes are a uint8
+  (``qweight[n, c] = sum_j q[n, 8c + j] << 4j``; per channel K need not be a
+  multiple of 8, and the last word's unused nibbles are zero); INT8 codes are a uint8
   ``[N, K]`` array.
 * ``x = default_rng([seed, M, 1]).standard_normal((M, K), float32)``, then
   optionally ``round(0.01 K)`` outlier columns (drawn from the same generator
@@ -80,8 +81,11 @@ class QuantisedWeights:
 def pack_w4(q: np.ndarray) -> np.ndarray:
     """Pack INT4 codes [N, K] eight per uint32, low nibble first along K."""
     n, k = q.shape
-    q = q.astype(np.uint32).reshape(n, k // 8, 8)
-    out = np.zeros((n, k // 8), dtype=np.uint32)
+    k8 = (k + 7) // 8 * 8  # a last, partial word keeps its unused nibbles zero
+    qp = np.zeros((n, k8), dtype=np.uint32)
+    qp[:, :k] = q
+    q = qp.reshape(n, k8 // 8, 8)
+    out = np.zeros((n, k8 // 8), dtype=np.uint32)
     for j in range(8):
         out |= q[:, :, j] << np.uint32(4 * j)
     return out
@@ -92,8 +96,8 @@ def quantise(w: np.ndarray, bits: int, group: int) -> QuantisedWeights:
     w = np.ascontiguousarray(w, dtype=np.float32)
     n, k = w.shape
     g = k if group == 0 else group
-    if k % 8 or k % g:
-        raise ValueError(f"K={k} must be a multiple of 8 and of the group {g}")
+    if (k % 8 and group != 0) or k % g:
+        raise ValueError(f"K={k} must be a multiple of the group {g} (and of 8 unless per channel)")
     qmax = np.float32(2**bits - 1)
     wg = w.reshape(n, k // g, g)
     mn = wg.min(axis=2)

@@ -17,11 +17,12 @@
  * Conventions shared by every call:
  *  - bits is 4 or 8.  group is 32, 64, any multiple of 128 that divides K,
  *    or 0 for per output channel (one group spanning all of K).  K must be
- *    a multiple of 8 and of the group.  1 <= N, K <= 32768 (Contributions 2:
+ *    a multiple of the group, and of 8 unless per channel.  1 <= N, K <= 32768 (Contributions 2:
  *    the layout stays valid for dimensions up to 32K).
  *  - BF16 values are passed as their uint16 bit patterns.
- *  - Natural-order inputs (host memory): INT4 qweight is uint32 [N, K/8],
- *    eight codes per word, low nibble first along K; INT8 qweight is uint8
+ *  - Natural-order inputs (host memory): INT4 qweight is uint32
+ *    [N, ceil(K/8)], eight codes per word, low nibble first along K (a last,
+ *    partial word keeps its unused nibbles zero); INT8 qweight is uint8
  *    [N, K]; scales uint16 [N, K/g]; zeros uint8 [N, K/g] (0..2^bits-1).
  *  - The caller allocates and owns every buffer.  The library allocates no
  *    memory; its only global state is cached device attributes, one
@@ -198,7 +199,11 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  * to run.
  * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),
  * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size; may
- * be NULL when that is 0).  1 <= M <= 8, else TF_ERR_UNSUPPORTED.
+ * be NULL when that is 0).  1 <= M <= 8, else TF_ERR_UNSUPPORTED.  With
+ * K % 8 != 0 (per channel) the stream GEMV takes the layer whatever its N,
+ * reading x element by element; its activations must fit in shared memory
+ * next to the weight ring (M * K up to about 64K elements), else
+ * TF_ERR_UNSUPPORTED.
  */
 int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,
@@ -218,8 +223,10 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
 /*
  * Workspace bytes tf_gemm needs on the current device for this layer and M
  * to split the K dimension of its last, partial wave of output tiles across
- * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters.  0
- * when the tiles fill whole waves.  Like the GEMV workspace it must be
+ * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters, 0
+ * when the tiles fill whole waves; plus, when K % 8 != 0 (per channel), a
+ * copy of x with rows padded to a multiple of 8 elements (a TMA tensor's
+ * rows must be multiples of 16 bytes), rewritten by every call.  Like the GEMV workspace it must be
  * zero-filled before its first use, and every tf_gemm that completes leaves
  * it zero-filled.  After a call that reported a device error
  * (tf_device_error nonzero) zero it again before reusing it.
@@ -236,6 +243,9 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  * SMs and their partial sums added in a fixed order (same result every run);
  * with workspace NULL (workspace_bytes ignored) every tile is computed whole
  * by one SM.  A workspace smaller than required gives TF_ERR_WORKSPACE.
+ * With K % 8 != 0 (per channel) the workspace is required (it holds the
+ * padded copy of x, made by a small kernel on the stream before the GEMM);
+ * NULL gives TF_ERR_WORKSPACE.
  */
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,

@@ -212,8 +212,11 @@ def unprepack(blob: np.ndarray):
                 zeros[s * UNIT_N + mrows, grp] = zv
     q = q[:N, :K]
     if bits == 4:
-        qr = q.reshape(N, K // 8, 8).astype(np.uint32)
-        qweight = np.zeros((N, K // 8), dtype=np.uint32)
+        K8 = (K + 7) // 8 * 8  # the last word's unused nibbles are zero
+        qr = np.zeros((N, K8), dtype=np.uint32)
+        qr[:, :K] = q
+        qr = qr.reshape(N, K8 // 8, 8)
+        qweight = np.zeros((N, K8 // 8), dtype=np.uint32)
         for i in range(8):
             qweight |= qr[:, :, i] << np.uint32(4 * i)
     else:

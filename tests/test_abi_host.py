@@ -39,6 +39,7 @@ def test_exports_every_declared_symbol():
 @pytest.mark.parametrize("N,K,bits,group", [
     (256, 512, 4, 128), (200, 192, 4, 64), (136, 200, 8, 0), (64, 96, 4, 32),
     (130, 256, 8, 128), (8, 8, 4, 0), (128, 1024, 4, 256), (300, 384, 8, 64), (72, 96, 8, 32),
+    (200, 1003, 4, 0), (130, 77, 8, 0), (17, 5, 4, 0), (33, 3, 8, 0),  # K % 8 != 0, per channel
 ])
 def test_prepack_matches_reference_layout(N, K, bits, group):
     qw = synth.make_weights(N, K, bits, group, 5)
@@ -77,7 +78,8 @@ def test_invalid_arguments_return_codes():
     lib = tf.lib()
     sz = ctypes.c_size_t()
     assert lib.tf_prepack_size(0, 128, 4, 128, ctypes.byref(sz)) == -1
-    assert lib.tf_prepack_size(128, 100, 4, 0, ctypes.byref(sz)) == -1       # K % 8
+    assert lib.tf_prepack_size(128, 100, 4, 0, ctypes.byref(sz)) == 0        # K % 8 != 0: per channel only
+    assert sz.value == 64 + 8 * 1 * 1072
     assert lib.tf_prepack_size(128, 256, 4, 96, ctypes.byref(sz)) == -2      # group 96
     assert lib.tf_prepack_size(128, 192, 4, 128, ctypes.byref(sz)) == -1     # K % g
     assert lib.tf_prepack_size(32769, 128, 4, 128, ctypes.byref(sz)) == -2   # > 32K

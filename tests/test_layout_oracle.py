@@ -38,6 +38,7 @@ def test_fragment_slots_follow_mma_register_order():
 @pytest.mark.parametrize("N,K,bits,group", [
     (256, 512, 4, 128), (200, 192, 4, 64), (136, 200, 8, 0), (64, 96, 4, 32),
     (130, 256, 8, 128), (8, 8, 4, 0), (128, 1024, 4, 256), (300, 384, 8, 64),
+    (200, 1003, 4, 0), (24, 77, 8, 0), (17, 5, 4, 0),  # K % 8 != 0, per channel
 ])
 def test_round_trip_identity(N, K, bits, group):
     qw = synth.make_weights(N, K, bits, group, 1)
@@ -144,3 +145,19 @@ def test_unit_sizes_are_aligned():
 def test_32k_geometry():
     S, kt, ub, total = L.blob_geometry(32768, 32768, 4, 128)
     assert (S, kt) == (2048, 256) and total == 64 + 2048 * 256 * 1072
+
+
+def test_partial_last_word_of_ragged_k():
+    """K = 5 per channel: one word per row, codes in its five low nibbles, the
+    three high nibbles unused (zero); unpack reads the codes in order, and the
+    blob's padding columns k >= 5 carry the row's zero point (exact zeros)."""
+    from oracle import tf_oracle
+    qweight = np.array([[0x00054321], [0x000FEDCB]], dtype=np.uint32)
+    np.testing.assert_array_equal(tf_oracle.unpack_w4(qweight, 5), [[1, 2, 3, 4, 5], [11, 12, 13, 14, 15]])
+    scales = np.full((2, 1), 0x3F80, np.uint16)  # 1.0
+    zeros = np.array([[3], [9]], np.uint8)
+    blob = L.prepack(qweight, scales, zeros, 2, 5, 4, 0)
+    r = L.unprepack(blob)
+    np.testing.assert_array_equal(r[0], qweight)
+    w = tf_oracle.dequant(tf_oracle.unpack_w4(qweight, 5), scales, zeros, 0)
+    np.testing.assert_array_equal(w, [[-2, -1, 0, 1, 2], [2, 3, 4, 5, 6]])
