@@ -224,9 +224,19 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+_RAW_STREAM = None
+
+
 def _stream_handle(stream) -> int:
+    """cudaStream_t of the given torch stream, else of the current one (without building a Stream object)."""
+    global _RAW_STREAM
+    if stream is not None:
+        return stream.cuda_stream
     torch = _torch()
-    return (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+    if _RAW_STREAM is None:
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None) or (
+            lambda dev: torch.cuda.current_stream(dev).cuda_stream)
+    return _RAW_STREAM(torch.cuda.current_device())
 
 
 def _workspace_args(W, M: int, kind: str, workspace):

@@ -1032,6 +1032,10 @@ int tf_gemv_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int
 
 static __device__ __align__(256) unsigned char tf_gemv_scratch[TF_GEMV_NOALLOC_SCRATCH_BYTES];
 
+// Bytes at the start of tf_gemv_scratch kept for the arrival counters: one
+// per (128-row block, warp), at most 256 x 8 for N <= 32768.
+constexpr size_t kNoallocCounterBytes = 16384;
+
 namespace {
 
 // Device address of tf_gemv_scratch on the current device (cached per device).
@@ -1049,6 +1053,16 @@ unsigned char* gemv_scratch_address() {
 
 }  // namespace
 
+namespace tf {
+
+int clear_noalloc_scratch() {
+  unsigned char* scratch = gemv_scratch_address();
+  if (!scratch) return TF_ERR_CUDA;
+  return cudaMemset(scratch, 0, TF_GEMV_NOALLOC_SCRATCH_BYTES) == cudaSuccess ? TF_OK : TF_ERR_CUDA;
+}
+
+}  // namespace tf
+
 extern "C" {
 
 int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits, int group, const uint16_t* x,
@@ -1065,16 +1079,21 @@ int tf_gemv_noalloc(const void* blob, size_t blob_bytes, int N, int K, int bits,
   GemvPlan P;
   rc = gemv_plan(G, M, &P);
   if (rc) return rc;
-  if (gemv_scratch_bytes(P) > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES) return TF_ERR_SCRATCH_LIMIT;
+  // The arrival counters have a fixed region at the start of the array, the
+  // partial sums the rest: the counters are zero when the library is loaded,
+  // no layer's partial sums ever land on them, and every call that completes
+  // leaves the counters it used at zero (the last arriver of each row block
+  // resets its own), so no call has to clear them first.  A call cut short
+  // by a device error may leave them dirty: tf_device_error, which reports
+  // that error, zeroes the array.
+  if (P.counter_bytes > kNoallocCounterBytes ||
+      P.partial_bytes > (size_t)TF_GEMV_NOALLOC_SCRATCH_BYTES - kNoallocCounterBytes)
+    return TF_ERR_SCRATCH_LIMIT;
   if (P.slab) return run_gemv(G, P, blob, x, e, M, nullptr, nullptr, stream);
   unsigned char* scratch = gemv_scratch_address();
   if (!scratch) return TF_ERR_CUDA;
-  // The arrival counters must start at zero; a call cut short (device error)
-  // could have left them dirty, so clear them on the stream first.
-  unsigned char* counters = scratch + P.partial_bytes;
-  if (cudaMemsetAsync(counters, 0, P.counter_bytes, stream) != cudaSuccess) return TF_ERR_CUDA;
-  return run_gemv(G, P, blob, x, e, M, reinterpret_cast<float4*>(scratch),
-                  reinterpret_cast<unsigned*>(counters), stream);
+  return run_gemv(G, P, blob, x, e, M, reinterpret_cast<float4*>(scratch + kNoallocCounterBytes),
+                  reinterpret_cast<unsigned*>(scratch), stream);
 }
 
 }  // extern "C"

@@ -53,6 +53,8 @@ extern "C" int tf_device_error(unsigned int* code) {
   unsigned v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, tf::g_tf_error, sizeof v) != cudaSuccess) return TF_ERR_CUDA;
   if (cudaMemcpyToSymbol(tf::g_tf_error, &zero, sizeof zero) != cudaSuccess) return TF_ERR_CUDA;
+  // a call cut short may have left tf_gemv_noalloc's arrival counters dirty
+  if (v != 0 && tf::clear_noalloc_scratch() != TF_OK) return TF_ERR_CUDA;
   *code = v;
   return TF_OK;
 }

@@ -15,6 +15,9 @@ namespace tf {
 // Device address of the current device's error word (cached per device).
 unsigned* device_error_ptr();
 
+// Zero the current device's tf_gemv_noalloc scratch array (synchronous).
+int clear_noalloc_scratch();
+
 // The failure-detection test hook (tf_test_stall_copies): while `stall` is
 // set, kernels issue no weight or activation copies, and every bounded wait
 // gives up after wait_ns (4 s when the hook is off).

@@ -310,10 +310,13 @@ int tf_gemm_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before capturing a stream into a CUDA graph.
- *  - Every call on a device shares the one array and leaves its last
- *    contents behind; each call first clears the arrival counters on its
- *    stream.  Calls that overlap on the GPU (other streams, other host
- *    threads) race on the array: order them on one stream or use tf_gemv.
+ *  - Every call on a device shares the one array.  Its arrival counters are
+ *    zero when the library is loaded, and every call that completes leaves
+ *    them at zero, so no call clears them first.  A call cut short by a
+ *    device error may leave them dirty: tf_device_error, when it reports an
+ *    error, also clears the array.  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on the array: order them on one
+ *    stream or use tf_gemv.
  *  - A layer whose scratch would exceed TF_GEMV_NOALLOC_SCRATCH_BYTES is
  *    rejected with TF_ERR_SCRATCH_LIMIT (every N, K <= 32768 fits on GPUs
  *    with up to ~200 SMs).
@@ -343,6 +346,8 @@ int tf_test_stall_copies(int stall, unsigned int timeout_us);
  * (producer, dequant, MMA, epilogue, drain), 0x600 a tile or slab GEMV wait,
  * 0x700 a stream GEMV wait, 0x800 the device blob's header does not match
  * the call (nothing written).  The first code since the last read is kept.
+ * When the code is nonzero it also zeroes the tf_gemv_noalloc scratch array
+ * of the device (a call cut short may have left its counters dirty).
  */
 int tf_device_error(unsigned int* code);
 

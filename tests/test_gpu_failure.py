@@ -39,6 +39,7 @@ CASES = [
     ("gemv", 3000, 2048, 8, 0, 3, {0x700}),
     ("gemv", 1024, 2048, 4, 128, 1, {0x600}),           # tile GEMV (fewer slabs than SMs)
     ("gemv", 4096, 2048, 4, 32, 1, {0x600}),            # slab GEMV (groups of 32)
+    ("gemv_noalloc", 1024, 2048, 4, 128, 1, {0x600}),   # tile GEMV on the fixed scratch array
     ("gemm", 4096, 4096, 4, 128, 256, {0x100, 0x200, 0x300, 0x400, 0x500}),
     ("gemm", 2048, 1024, 8, 0, 64, {0x100, 0x200, 0x300, 0x400, 0x500}),
 ]
@@ -51,7 +52,7 @@ def test_wait_runs_out_and_context_survives(call, N, K, bits, group, M, codes):
     qw, W = layer(N, K, bits, group, 61)
     xb = synth.make_activations(M, K, 61)
     x = to_dev_bf16(xb)
-    fn = tf.gemv if call == "gemv" else tf.gemm
+    fn = {"gemv": tf.gemv, "gemm": tf.gemm, "gemv_noalloc": tf.gemv_noalloc}[call]
     fn(W, x)  # the lazy set-up (attributes, workspace) outside the stalled call
     torch.cuda.synchronize()
     assert tf.device_error() == 0
