@@ -72,7 +72,7 @@ struct GemmArgs {
   uint64_t wait_ns;           // limit of every wait
   int stall;                  // failure-detection test: the producers issue no copies
   int y_tma;                  // 1: whole tiles of a plain y leave through shared-memory staging and TMA stores
-  int off_op, off_epi, off_bar;  // byte offsets in the 1024-aligned dynamic smem
+  int off_p, off_op, off_epi, off_bar;  // byte offsets in the 1024-aligned dynamic smem
 };
 
 // Token m's biased sum v of this thread's row n, through the epilogue.  All
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
           ok = mbar_wait(B.empty_p + 8 * ps, pph ^ 1, err, kErrProducerWait, a.wait_ns);
           if (!ok) break;
-          const uint32_t dst = sbase + (uint32_t)(ps * a.tile_bytes);
+          const uint32_t dst = sbase + (uint32_t)(a.off_p + ps * a.tile_bytes);
           if (!a.stall) {
             mbar_arrive_expect_tx(B.full_p + 8 * ps, (uint32_t)a.tile_bytes);
             if (BITS == 4)
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       for (int kt = wk.kb; kt < wk.ke && ok; ++kt) {
         ok = mbar_wait(B.full_p + 8 * ps, pph, err, kErrDequantWait, a.wait_ns);
         if (!ok) break;
-        const uint8_t* pk = smem + (size_t)ps * a.tile_bytes;
+        const uint8_t* pk = smem + a.off_p + (size_t)ps * a.tile_bytes;
         const uint32_t sp = *reinterpret_cast<const uint32_t*>(pk + s_off);
         uint32_t lo[8], hi[8];
         if (BITS == 4) {
@@ -556,6 +556,7 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P
   GemmArgs& a = P->a;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
   a.tile_bytes = kSlabsPerTile * G.unit_bytes;
+  if (a.tile_bytes % 128 != 0) return TF_ERR_UNSUPPORTED;  // each packed stage starts 128-byte aligned
   a.BN = M >= 256 ? 256 : (M + 15) / 16 * 16;
   a.MT = (M + a.BN - 1) / a.BN;
   a.ntiles = G.NB * a.MT;
@@ -563,15 +564,20 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P
   // y as a TMA tensor needs rows of a multiple of 16 bytes (and a plain y)
   a.y_tma = G.N % 8 == 0 && epi_mode == kEpiPlain ? 1 : 0;
   const int epi = a.y_tma ? kEpiStageBytes : 0;
+  // The operand ring (1024-byte aligned stages for the 128-byte swizzle)
+  // comes first at the aligned base, the packed ring (128-byte aligned tiles)
+  // right after it: at BN = 256 that leaves room for a third packed tile,
+  // which the weights' latency needs (+3-4 % at M = 2048 against two).
   a.OPS = 0;
   for (int ops = 4; ops >= 2 && a.OPS == 0; --ops)
     for (int p = 4; p >= 2; --p) {
-      const int off_op = (p * a.tile_bytes + 1023) / 1024 * 1024;
-      const int off_epi = off_op + ops * op_stage;
+      const int off_op = 0;
+      const int off_p = ops * op_stage;
+      const int off_epi = (off_p + p * a.tile_bytes + 127) / 128 * 128;
       const int off_bar = off_epi + epi;
       const size_t smem = 1024 + off_bar + 256;
       if (smem <= (size_t)kMaxSmem) {
-        a.P = p; a.OPS = ops; a.off_op = off_op; a.off_epi = off_epi; a.off_bar = off_bar;
+        a.P = p; a.OPS = ops; a.off_p = off_p; a.off_op = off_op; a.off_epi = off_epi; a.off_bar = off_bar;
         P->smem = smem;
         break;
       }
