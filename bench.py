@@ -427,7 +427,8 @@ def run_ours(args, rank, world):
                 barrier()
                 te = time.perf_counter()
             step_graphs[s % copies].replay()
-            stream.synchronize()
+            while not stream.query():  # the step's result is on the host (poll rather than sleep)
+                pass
     e2e_ms = max_over_ranks((time.perf_counter() - te) * 1e3 / e2e_steps)
     e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
     eager_value = job_rate(step_bytes, world, eager_ms) / 1e9
@@ -532,7 +533,7 @@ def run_ours(args, rank, world):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "path": "pinned host x of the four layers -> device (one copy), tf_gemv x4 through the "
                         "Python binding, the four y -> pinned host (one copy); the step captured once into a "
-                        "CUDA graph and replayed, with a stream synchronise, every step",
+                        "CUDA graph and replayed every step, the host polling the stream until it is done",
                 "eager": {"value": round(eager_value, 1), "ms_per_step": round(eager_ms, 4),
                           "path": "the same step issued from Python every step"}},
         "gpu_launches": args.steps * len(DECODE),
