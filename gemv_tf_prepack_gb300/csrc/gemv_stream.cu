@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   float* red = reinterpret_cast<float*>(smem + a.off_red);
   const uint32_t full = sbase + (uint32_t)a.off_ctl;      // [16 warps][NS] mbarriers
   int* flags = reinterpret_cast<int*>(smem + a.off_ctl + 8 * kSW * NS);  // [0] a wait ran out, [1] bad header
+  float* bias_s = reinterpret_cast<float*>(smem + a.off_ctl + 8 * kSW * NS + 8);  // this CTA's rows' bias
 
   // This CTA's whole slabs [s0, s0 + nslabs), i.e. units [u0, u1), and this
   // warp's run [g0, g0 + nu) of them (memory order).
@@ -402,6 +403,12 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
   if (lane == 0)  // every warp requests its own stages
     for (int i = 0; i < npre; ++i)
       warp_fill<BITS, GPT>(a, ring + (uint32_t)(i * SB), wbar + 8u * i, g0 + i * S, nu - i * S < S ? nu - i * S : S);
+  // the bias, static like the weights, is read before the dependency too
+  if (a.epi.bias)
+    for (int i = threadIdx.x; i < nslabs * kSlabN; i += kSThreads) {
+      const int nn = s0 * kSlabN + i;
+      bias_s[i] = nn < a.N ? bf16_bits_to_float(a.epi.bias[nn]) : 0.f;
+    }
   griddep_wait();
   // Activations: each half warp takes one 128-column block of one token at
   // a time (lane l: columns 8l .. 8l + 7), straight into registers: its
@@ -600,9 +607,12 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_stream_kernel(const StreamA
     const float v = parked(sl, idx);
     if (gate) {  // gate row nn (row < 8) with its up row nn + 8
       const float u = parked(sl, idx + 8 * Mp);
-      epi_put_gate(a.epi, tok, nn, epi_biased(a.epi, nn, v), epi_biased(a.epi, nn + 8, BITS == 4 ? u * 0.0625f : u));
+      const float ub = BITS == 4 ? u * 0.0625f : u;
+      const float* b = bias_s + sl * kSlabN + row;
+      epi_put_gate(a.epi, tok, nn, a.epi.bias ? v + b[0] : v, a.epi.bias ? ub + b[8] : ub);
     } else {
-      epi_put(a.epi, tok, nn, epi_biased(a.epi, nn, BITS == 4 && row >= 8 ? v * 0.0625f : v));
+      const float vb = BITS == 4 && row >= 8 ? v * 0.0625f : v;
+      epi_put(a.epi, tok, nn, a.epi.bias ? vb + bias_s[sl * kSlabN + row] : vb);
     }
   }
 }
@@ -636,7 +646,7 @@ int stream_plan(const Geometry& G, int M, StreamPlan* P) {
     const int stage = warp_stage_units(G.bits, half != 0) * G.unit_bytes;
     for (int ns = TF_STREAM_NS_MAX; ns >= 2; --ns) {
       const int ring = (kSW * ns * stage + 127) / 128 * 128;
-      const int ctl = 8 * kSW * ns + 8;
+      const int ctl = 8 * kSW * ns + 8 + S.max_slabs * kSlabN * 4;  // mbarriers, flags, the rows' bias
       const size_t smem = 128 + (size_t)ring + xres + xs + red + ctl;
       if (smem <= (size_t)kSmemMax) {
         S.half = half;

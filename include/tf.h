@@ -34,6 +34,10 @@
  *    TF_ERR_CUDA return means the launch itself failed.
  *  - Calls are thread-safe.  Two device calls that share a workspace must
  *    not run concurrently.
+ *  - The GEMV kernels start early under programmatic dependent launch: they
+ *    read the blob and the bias before waiting for the kernel launched just
+ *    before them on the stream (x, y and the workspace only after it).  The
+ *    weights and the bias must therefore not be written by that kernel.
  *  - Device state (the error word, the scratch array of tf_gemv_noalloc,
  *    cached device attributes) is looked up once per device, in the context
  *    current at the first call: the device's primary context, which the
