@@ -191,3 +191,60 @@ def test_header_serves_a_plain_c_client(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     assert out[:4] == [str(tf.version()), "0", str(tf.prepack_size(4096, 4096, 4, 128)), "-2"]
     assert out[4] == "TF_ERR_UNSUPPORTED:"
+
+
+def test_plain_c_client_packs_a_gate_up_layer(tmp_path):
+    """A C11 program builds a gate/up blob with tf_prepack_gate_up and reads it
+    back with tf_blob_info; the bytes equal the Python binding's."""
+    import os
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = next((d for d in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda")
+                     if d and os.path.exists(os.path.join(d, "include", "cuda_runtime_api.h"))), None)
+    if cuda_inc is None:
+        pytest.skip("cuda_runtime_api.h not found")
+    F, K = 8, 24  # K % 8 == 0 here; per channel
+    g = synth.make_weights(F, K, 4, 0, 11)
+    u = synth.make_weights(F, K, 4, 0, 12)
+    arrays = {"gq": g.qweight, "gs": g.scales, "gz": g.zeros, "uq": u.qweight, "us": u.scales, "uz": u.zeros}
+    for name, a in arrays.items():
+        np.ascontiguousarray(a).tofile(tmp_path / f"{name}.bin")
+    size = tf.prepack_size(2 * F, K, 4, 0)
+    src = tmp_path / "gate_up.c"
+    src.write_text(
+        '#include "tf.h"\n#include <stdio.h>\n#include <stdlib.h>\n'
+        "static void* load(const char* path, size_t n) {\n"
+        "  void* p = malloc(n); FILE* f = fopen(path, \"rb\");\n"
+        "  if (!f || fread(p, 1, n, f) != n) exit(3);\n"
+        "  fclose(f); return p;\n}\n"
+        "int main(int argc, char** argv) {\n"
+        "  (void)argc;\n"
+        f"  const int F = {F}, K = {K};\n"
+        "  char path[4096];\n"
+        "#define LOAD(name, n) (snprintf(path, sizeof path, \"%s/%s.bin\", argv[1], name), load(path, n))\n"
+        "  void* gq = LOAD(\"gq\", (size_t)F * (K / 8) * 4); void* uq = LOAD(\"uq\", (size_t)F * (K / 8) * 4);\n"
+        "  uint16_t* gs = LOAD(\"gs\", (size_t)F * 2); uint16_t* us = LOAD(\"us\", (size_t)F * 2);\n"
+        "  uint8_t* gz = LOAD(\"gz\", (size_t)F); uint8_t* uz = LOAD(\"uz\", (size_t)F);\n"
+        f"  size_t bytes = {size};\n"
+        "  unsigned char* blob = malloc(bytes);\n"
+        "  int rc = tf_prepack_gate_up(gq, gs, gz, uq, us, uz, F, K, 4, 0, blob, bytes);\n"
+        "  int n = 0, k = 0, bits = 0, group = -1;\n"
+        "  int rc2 = tf_blob_info(blob, bytes, &n, &k, &bits, &group);\n"
+        "  unsigned long sum = 0;\n"
+        "  for (size_t i = 0; i < bytes; ++i) sum = sum * 31u + blob[i];\n"
+        "  printf(\"%d %d %d %d %d %d %lu\\n\", rc, rc2, n, k, bits, group, sum);\n"
+        "  return rc;\n}\n")
+    exe = tmp_path / "gate_up"
+    pkg = os.path.dirname(tf.lib_path)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.dirname(tf.HEADER), "-I",
+                    os.path.join(cuda_inc, "include"), str(src), "-o", str(exe), "-L", pkg, "-ltf",
+                    "-Wl,-rpath," + pkg], check=True, capture_output=True)
+    out = subprocess.run([str(exe), str(tmp_path)], capture_output=True, text=True, check=True).stdout.split()
+    want = tf.prepack_gate_up((g.qweight, g.scales, g.zeros), (u.qweight, u.scales, u.zeros), F, K, 4, 0)
+    s = 0
+    for b in want.tobytes():
+        s = (s * 31 + b) % (1 << 64)
+    assert out[:6] == ["0", "0", str(2 * F), str(K), "4", "0"]
+    assert int(out[6]) == s
