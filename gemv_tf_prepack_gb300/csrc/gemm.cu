@@ -17,8 +17,10 @@
 //                K = 16) from one thread, accumulating in tensor memory;
 //                two accumulators let the epilogue of one tile overlap the
 //                MMAs of the next;
-//   warps 2..5   read the accumulator with tcgen05.ld, round to BF16 and
-//                store y.
+//   warps 2..5   read the accumulator with tcgen05.ld, add the bias, round
+//                to BF16 and store y through the epilogue (plain y by TMA
+//                tile stores; the SiLU gate and the QKV split, or N % 8 != 0,
+//                element by element).
 // Each dequantised 128 x 64 weight slab feeds BN/16 * 4 MMAs, i.e. it is
 // reused across all BN tokens of the tile.  CTAs are persistent (one per
 // SM) and walk output tiles with the token index fastest, so CTAs that run

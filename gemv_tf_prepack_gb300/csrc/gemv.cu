@@ -9,12 +9,18 @@
 // fragments go straight into mma.sync so that the tensor cores do the
 // multiply-accumulate instead of CUDA-core FMAs.
 //
-// Two kernels share that inner step (one 16-row x 128-column unit per warp):
-//  * slab GEMV, for layers with at least as many 16-row slabs as SMs whose
-//    activations fit in shared memory: each CTA owns whole slabs over all of
-//    K, its eight (or sixteen) warps split K, and a slab's partial sums meet
-//    in shared memory.  No CTA waits on another, so a layer ends as soon as
-//    its last slab is done.
+// The layers with at least one 16-row slab per SM and groups of 64, any
+// multiple of 128 or per channel (every decode projection of a Llama-class
+// model) go to the stream GEMV of gemv_stream.cu, which skips the per-weight
+// BF16 rounding.  This file holds the entry points, the routing, and the two
+// GEMVs for the other layers, which dequantise each weight to BF16 in
+// registers (bit-exact, as tf_dequant) and share one inner step (one 16-row
+// x 128-column unit per warp):
+//  * slab GEMV, for groups of 32 on layers with at least as many 16-row slabs
+//    as SMs whose activations fit in shared memory: each CTA owns whole slabs
+//    over all of K, its eight (or sixteen) warps split K, and a slab's partial
+//    sums meet in shared memory.  No CTA waits on another, so a layer ends as
+//    soon as its last slab is done.
 //  * tile GEMV, for the rest (few rows, short K, or activations too large to
 //    stay resident): K is split across CTAs too; a 128-row block shared by
 //    several CTAs is summed by the last of them, in a fixed order, from FP32
