@@ -34,6 +34,7 @@ FORMATS = [
     (256, 512, 4, 128), (200, 192, 4, 64), (136, 200, 8, 0), (64, 96, 4, 32),
     (130, 256, 8, 128), (8, 8, 4, 0), (128, 1024, 4, 256), (300, 384, 8, 64), (72, 96, 8, 32),
     (1000, 1016, 4, 0), (384, 4096, 4, 128),
+    (1, 8, 4, 0), (3, 256, 8, 64),  # a single output row; three rows of one partial slab
 ]
 
 
