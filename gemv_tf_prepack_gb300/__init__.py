@@ -369,7 +369,10 @@ def gemm(W: Weights, x, y=None, workspace=None, stream=None, stream_k=True, bias
 
     With stream_k (default) the layer's cached workspace lets the last,
     partial wave of output tiles be split along K across all SMs; with
-    stream_k False every tile is computed whole by one SM.
+    stream_k False every tile is computed whole by one SM.  M <= 8 (K a
+    multiple of 8) runs on the slab or tile GEMV instead, with the same
+    per-weight BF16 rounding; stream_k False there passes no workspace, so
+    a layer whose GEMV needs one falls back to whole tensor-core tiles.
     """
     _check_x(W, x)
     M = x.shape[0]

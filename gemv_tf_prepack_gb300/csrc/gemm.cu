@@ -549,11 +549,16 @@ struct GemmPlan {
   GemmArgs a;
   size_t smem;
   int grid;
-  size_t ws_bytes, cnt_bytes;  // stream-K workspace: partial sums, then arrival counters
+  size_t ws_bytes;  // stream-K partial sums (0 without stream-K)
 };
 
+// Stream-K bytes of the workspace: the arrival counters in the first
+// kWorkspaceCounterBytes (as in every split-K workspace of the library), the
+// partial sums after them.
+inline size_t sk_scratch_bytes(const GemmPlan& P) { return P.ws_bytes ? kWorkspaceCounterBytes + P.ws_bytes : 0; }
+
 // stream_k: split the tiles of the last, partial wave (plus one whole wave)
-// along K; needs the workspace sized by ws_bytes + cnt_bytes.
+// along K; needs sk_scratch_bytes of workspace.
 int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P) {
   GemmArgs& a = P->a;
   a.N = G.N; a.K = G.K; a.M = M; a.KT = G.KT; a.g = G.g; a.group = G.group;
@@ -612,6 +617,7 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P
       }
     }
   }
+  if (sk > 0 && ((size_t)sk * sizeof(unsigned) > kWorkspaceCounterBytes)) sk = 0;  // not reached: sk <= SMs
   if (sk > 0) {
     a.dp_tiles = a.ntiles - sk;
     // with fewer k-iterations than CTAs, one k-iteration each for the first ones
@@ -619,12 +625,11 @@ int gemm_plan(const Geometry& G, int M, bool stream_k, int epi_mode, GemmPlan* P
     a.sk_ctas = iters < sk_ctas ? (int)iters : sk_ctas;
     P->grid = sms;
     P->ws_bytes = (size_t)a.sk_ctas * 2 * 128 * a.BN * sizeof(float);
-    P->cnt_bytes = ((size_t)sk * sizeof(unsigned) + 255) / 256 * 256;
   } else {
     a.dp_tiles = a.ntiles;
     a.sk_ctas = 1;
     P->grid = a.ntiles < sms ? a.ntiles : sms;
-    P->ws_bytes = P->cnt_bytes = 0;
+    P->ws_bytes = 0;
   }
   return TF_OK;
 }
@@ -648,7 +653,8 @@ int launch_gemm(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorM
 
 // Bytes of the activations copied to rows of a multiple of 8 elements
 // (K % 8 != 0, per channel only: a TMA tensor's rows must be multiples of
-// 16 bytes), kept in the caller's workspace after the stream-K part.
+// 16 bytes), kept in the caller's workspace after the counter region and
+// the stream-K partial sums.
 size_t padded_x_bytes(const Geometry& G, int M) {
   if (G.K % 8 == 0) return 0;
   const size_t k8 = (size_t)(G.K + 7) / 8 * 8;
@@ -676,14 +682,22 @@ int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int gr
   rc = check_epi(epi);
   if (rc) return rc;
   if (!aligned16(x) || !aligned16(workspace) || (epi.mode == kEpiPlain && !aligned16(epi.y))) return TF_ERR_ALIGNMENT;
+  // Up to 8 tokens the slab or tile GEMV takes the product (one 8-token
+  // MMA column per weight fragment, every weight read once) when the
+  // workspace it needs is given, or it needs none: the tensor-memory
+  // pipeline below spends about a microsecond per k-step whatever M is.
+  size_t small_need = 0;
+  if (M <= 8 && small_m_workspace(G, M, &small_need) == TF_OK && (workspace || small_need == 0))
+    return run_small_m(G, blob, x, epi, M, workspace, workspace_bytes, stream);
   GemmPlan P;
   rc = gemm_plan(G, M, workspace != nullptr, epi.mode, &P);
   if (rc) return rc;
   const size_t pad_bytes = padded_x_bytes(G, M);
+  const size_t pad_off = kWorkspaceCounterBytes + P.ws_bytes;
   if (pad_bytes && !workspace) return TF_ERR_WORKSPACE;  // the padded activations live there
-  if (workspace && workspace_bytes < P.ws_bytes + P.cnt_bytes + pad_bytes) return TF_ERR_WORKSPACE;
-  P.a.ws = static_cast<float*>(workspace);
-  P.a.cnt = P.ws_bytes ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.ws_bytes) : nullptr;
+  if (workspace && workspace_bytes < (pad_bytes ? pad_off + pad_bytes : sk_scratch_bytes(P))) return TF_ERR_WORKSPACE;
+  P.a.cnt = P.ws_bytes ? static_cast<unsigned*>(workspace) : nullptr;
+  P.a.ws = P.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceCounterBytes) : nullptr;
   P.a.units = static_cast<const uint8_t*>(blob) + kHeaderBytes;
   P.a.epi = epi;
   P.a.err = device_error_ptr();
@@ -695,7 +709,7 @@ int gemm_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int gr
   const uint16_t* xa = x;
   int ka = K;
   if (pad_bytes) {
-    uint16_t* xp = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + P.ws_bytes + P.cnt_bytes);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + pad_off);
     ka = (K + 7) / 8 * 8;
     const size_t total = (size_t)M * ka;
     const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
@@ -740,7 +754,10 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
   GemmPlan P;
   rc = gemm_plan(G, M, true, kEpiPlain, &P);
   if (rc) return rc;
-  *bytes = P.ws_bytes + P.cnt_bytes + padded_x_bytes(G, M);
+  const size_t pad = padded_x_bytes(G, M);
+  *bytes = pad ? kWorkspaceCounterBytes + P.ws_bytes + pad : sk_scratch_bytes(P);
+  size_t small = 0;
+  if (M <= 8 && small_m_workspace(G, M, &small) == TF_OK) *bytes = small;  // the slab or tile GEMV takes these
   return TF_OK;
 }
 

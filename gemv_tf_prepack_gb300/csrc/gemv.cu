@@ -366,10 +366,12 @@ __device__ __forceinline__ void next_segment(Segment& g, int ntile, int KT) {
 // activation slices) into stage s.  Called by all lanes of one warp: lane i
 // copies unit i % 8 of tile i / 8; lane 0 arms the barrier and loads the
 // activations.  The activations are read only once the grid dependency has
-// resolved (x).
+// resolved (x).  `issued` counts the fills whose copies were started (for
+// the drain after a wait that ran out).
 template <int BITS, int GPT, int TPS>
 __device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap* tmx, uint32_t sbase, uint32_t full,
-                                           long long t0, int ntile, int f, int s, bool weights, bool x, int lane) {
+                                           long long t0, int ntile, int f, int s, bool weights, bool x, int lane,
+                                           int* issued) {
   constexpr int UB = unit_bytes_gpu(BITS, GPT);
   const int i = f * TPS;
   const int n = ntile - i < TPS ? ntile - i : TPS;
@@ -378,7 +380,10 @@ __device__ __forceinline__ void issue_fill(const GemvArgs& a, const CUtensorMap*
   const uint32_t bar = full + 8u * s;
   const uint32_t dst = sbase + (uint32_t)(s * a.stage_bytes);
   if (weights) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n * ((uint32_t)(kSlabsPerTile * UB) + x_bytes));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)n * ((uint32_t)(kSlabsPerTile * UB) + x_bytes));
+      atomicMax(issued, f + 1);
+    }
     __syncwarp();
     if (lane < n * kSlabsPerTile) {
       const int j = lane / kSlabsPerTile, mb = lane % kSlabsPerTile;
@@ -414,6 +419,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   // per-stage release counters: the last warp to hand a stage back refills it
   unsigned* released = reinterpret_cast<unsigned*>(smem + a.NS * a.stage_bytes + 16 * a.NS);
   int* bad = reinterpret_cast<int*>(released + a.NS);  // the blob's header does not match the call
+  int* issued = bad + 1;                               // fills whose copies were started
+  int* dead = bad + 2;                                 // a wait ran out
   const int npre = nfill < a.NS ? nfill : a.NS;
   uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
   if (threadIdx.x == 0) {
@@ -423,6 +430,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
       mbar_init(empty + 8 * i, kGemvWarps);
       released[i] = 0;
     }
+    *issued = 0;
+    *dead = 0;
     mbar_init_fence();
   }
   __syncthreads();
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     }
     // static weights first, before the grid dependency resolves
     for (int f = 0; f < npre; ++f)
-      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, true, false, lane);
+      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, true, false, lane, issued);
   }
   // y, x and the workspace may still be in use by the previous grid
   griddep_wait();
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   }
   if (warp == 0)
     for (int f = 0; f < npre; ++f)
-      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true, lane);
+      issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f, f, false, true, lane, issued);
   __syncthreads();
   // With a header that does not match, the stream still runs to the end (so
   // that every copy lands) but nothing is written.
@@ -464,7 +473,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
   int s = 0;
   uint32_t lap = 0;
   for (int f = 0; f < nfill; ++f) {
-    if (!warp_wait(full + 8 * s, lap & 1u, a.err, a.wait_ns)) break;
+    if (!warp_wait(full + 8 * s, lap & 1u, a.err, a.wait_ns)) {
+      if (lane == 0) atomicExch(dead, 1);
+      break;
+    }
     const int i0 = f * kTilesPerStage;
     const int n = ntile - i0 < kTilesPerStage ? ntile - i0 : kTilesPerStage;
     const uint8_t* st = smem + s * a.stage_bytes;
@@ -488,7 +500,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
             }
           }
           if (__shfl_sync(0xFFFFFFFFu, refill, 0))
-            issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true, lane);
+            issue_fill<BITS, GPT, kTilesPerStage>(a, &tmx, sbase, full, t0, ntile, f + a.NS, s, true, true, lane,
+                                                  issued);
         }
         mma_unit(R, xs, acc);
         if (i0 + j == seg.end) {
@@ -514,6 +527,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     __syncwarp();
     publish_segment(a, pending0, warp, lane);
     if (npending > 1) publish_segment(a, pending1, warp, lane);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *dead) {
+    // A wait ran out: let the copies still in flight land before the CTA's
+    // shared memory goes away.  A fill is started only after every warp has
+    // handed back the fill NS before it, so only the last NS started fills
+    // can be outstanding.
+    const int n_iss = *issued;
+    for (int f = n_iss > a.NS ? n_iss - a.NS : 0; f < n_iss; ++f)
+      mbar_wait(full + 8 * (f % a.NS), (uint32_t)(f / a.NS) & 1u, a.err, kErrGemvWait, kGemvDrainNs);
   }
 }
 
@@ -853,12 +876,17 @@ inline int gemv_plan(const Geometry& Gm, int M, GemvPlan* P) {
   P->counter_bytes = ((size_t)Gm.NB * 8 * sizeof(unsigned) + 255) / 256 * 256;
   P->x_off = (TPS * kSlabsPerTile * Gm.unit_bytes + 127) / 128 * 128;
   P->stage_bytes = P->x_off + TPS * M * 256;
-  P->NS = clampi(kGemvSmemBudget / P->stage_bytes, 2, 6);
-  P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS + 4;
+  // ring + control words (barriers, release counters, header / issued / dead)
+  P->NS = clampi((kGemvSmemBudget - 12) / (P->stage_bytes + 20), 2, 6);
+  P->smem = 128 + (size_t)P->NS * P->stage_bytes + 16 * P->NS + 4 * P->NS + 12;
   return TF_OK;
 }
 
-inline size_t gemv_scratch_bytes(const GemvPlan& P) { return P.slab ? 0 : P.partial_bytes + P.counter_bytes; }
+// Workspace of the tile GEMV: the arrival counters in the first
+// kWorkspaceCounterBytes, the partial sums after them.
+inline size_t gemv_scratch_bytes(const GemvPlan& P) {
+  return P.slab ? 0 : kWorkspaceCounterBytes + P.partial_bytes;
+}
 
 template <int BITS, int GPT>
 int launch_tile(const CUtensorMap& map, const GemvArgs& a, size_t smem, cudaStream_t s) {
@@ -941,12 +969,37 @@ int gemv_epi(const void* blob, size_t blob_bytes, int N, int K, int bits, int gr
   if (rc) return rc;
   const size_t need = gemv_scratch_bytes(P);
   if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
-  return run_gemv(G, P, blob, x, epi, M, static_cast<float4*>(workspace),
-                  need ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + P.partial_bytes) : nullptr,
-                  stream);
+  return run_gemv(G, P, blob, x, epi, M,
+                  need ? reinterpret_cast<float4*>(static_cast<char*>(workspace) + kWorkspaceCounterBytes) : nullptr,
+                  static_cast<unsigned*>(workspace), stream);
 }
 
 }  // namespace
+
+// tf_gemm for M <= 8: the slab or tile GEMV (never the stream GEMV, whose
+// sums skip the per-weight rounding that tf_gemm keeps).
+int small_m_workspace(const Geometry& G, int M, size_t* bytes) {
+  if (M > 8) return TF_ERR_UNSUPPORTED;
+  GemvPlan P;
+  const int rc = gemv_plan(G, M, &P);
+  if (rc) return rc;
+  *bytes = gemv_scratch_bytes(P);
+  return TF_OK;
+}
+
+int run_small_m(const Geometry& G, const void* blob, const uint16_t* x, const Epi& epi, int M, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+  if (M > 8) return TF_ERR_UNSUPPORTED;
+  GemvPlan P;
+  const int rc = gemv_plan(G, M, &P);
+  if (rc) return rc;
+  const size_t need = gemv_scratch_bytes(P);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return TF_ERR_WORKSPACE;
+  return run_gemv(G, P, blob, x, epi, M,
+                  need ? reinterpret_cast<float4*>(static_cast<char*>(workspace) + kWorkspaceCounterBytes) : nullptr,
+                  static_cast<unsigned*>(workspace), stream);
+}
+
 }  // namespace tf
 
 using namespace tf;
@@ -1038,9 +1091,10 @@ int tf_gemv_qkv(const void* blob, size_t blob_bytes, int N, int K, int bits, int
 
 static __device__ __align__(256) unsigned char tf_gemv_scratch[TF_GEMV_NOALLOC_SCRATCH_BYTES];
 
-// Bytes at the start of tf_gemv_scratch kept for the arrival counters: one
-// per (128-row block, warp), at most 256 x 8 for N <= 32768.
-constexpr size_t kNoallocCounterBytes = 16384;
+// Bytes at the start of tf_gemv_scratch kept for the arrival counters (one
+// per 128-row block and warp, at most 256 x 8 for N <= 32768), as in a
+// caller's workspace.
+constexpr size_t kNoallocCounterBytes = kWorkspaceCounterBytes;
 
 namespace {
 

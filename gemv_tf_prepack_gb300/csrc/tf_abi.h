@@ -89,6 +89,20 @@ int stream_plan(const Geometry& G, int M, StreamPlan* P);
 int run_stream(const Geometry& G, const StreamPlan& P, const void* blob, const uint16_t* x, const Epi& epi, int M,
                cudaStream_t stream);
 
+// Split-K workspaces (tf_gemv, tf_gemm, the no-alloc scratch) keep their
+// arrival counters in this many bytes at the start and the partial sums
+// after them, so that no layer's partial sums ever land on another layer's
+// counters: one workspace can serve layers of any shape.
+constexpr size_t kWorkspaceCounterBytes = 16384;
+
+// tf_gemm for 1 <= M <= 8 on the slab or tile GEMV of gemv.cu, which keep
+// tf_gemm's per-weight BF16 rounding.  small_m_workspace gives the
+// workspace bytes (0 for the slab GEMV), or UNSUPPORTED when the layer is
+// not theirs (K % 8 != 0, M > 8).
+int small_m_workspace(const Geometry& G, int M, size_t* bytes);
+int run_small_m(const Geometry& G, const void* blob, const uint16_t* x, const Epi& epi, int M, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream);
+
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Streaming multiprocessors of the current device (cached per device).

@@ -34,6 +34,13 @@
  *    TF_ERR_CUDA return means the launch itself failed.
  *  - Calls are thread-safe.  Two device calls that share a workspace must
  *    not run concurrently.
+ *  - Workspaces (tf_gemv, tf_gemm) keep their arrival counters in the first
+ *    16384 bytes and everything else after them, and every call that
+ *    completes leaves those counters at zero.  So one workspace, zero-filled
+ *    once and at least as large as the largest size asked for, can serve
+ *    calls of any layer and any M, tf_gemv and tf_gemm alike, in turn on one
+ *    stream.  After a call that reported a device error (tf_device_error
+ *    nonzero), zero it again.
  *  - The GEMV kernels start early under programmatic dependent launch: they
  *    read the blob and the bias before waiting for the kernel launched just
  *    before them on the stream (x, y and the workspace only after it).  The
@@ -171,13 +178,15 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
 
 /*
  * Workspace bytes tf_gemv needs on the current device for this layer and M
- * (split-K partial sums plus per-block arrival counters; 0 for layers with
- * at least one 16-row slab per SM, whose blocks each stream whole slabs).
- * The workspace must be zero-filled before its first use; every tf_gemv
- * that completes leaves the arrival counters at zero again (the partial sums
- * are always written before they are read), so one workspace can be reused
- * by calls ordered on one stream.  After a call that reported a device error
- * (tf_device_error nonzero) zero the workspace again before reusing it.
+ * (16384 bytes of per-block arrival counters, then the split-K partial
+ * sums; 0 for layers with at least one 16-row slab per SM, whose blocks
+ * each stream whole slabs).  The workspace must be zero-filled before its
+ * first use; every tf_gemv that completes leaves the arrival counters at
+ * zero again (the partial sums are always written before they are read), so
+ * one workspace can be reused by calls ordered on one stream, for any layer
+ * (see the workspace rule above).  After a call that reported a device
+ * error (tf_device_error nonzero) zero the workspace again before reusing
+ * it.
  */
 int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
@@ -225,15 +234,18 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
                  size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * Workspace bytes tf_gemm needs on the current device for this layer and M
- * to split the K dimension of its last, partial wave of output tiles across
- * all SMs (stream-K): FP32 partial sums plus per-tile arrival counters, 0
- * when the tiles fill whole waves; plus, when K % 8 != 0 (per channel), a
- * copy of x with rows padded to a multiple of 8 elements (a TMA tensor's
- * rows must be multiples of 16 bytes), rewritten by every call.  Like the GEMV workspace it must be
- * zero-filled before its first use, and every tf_gemm that completes leaves
- * it zero-filled.  After a call that reported a device error
- * (tf_device_error nonzero) zero it again before reusing it.
+ * Workspace bytes tf_gemm needs on the current device for this layer and M.
+ * M <= 8 (K % 8 == 0): what the slab or tile GEMV behind it needs, as
+ * tf_gemv_workspace_size (0 on layers with a 16-row slab per SM).  Else, to
+ * split the K dimension of its last, partial wave of output tiles across
+ * all SMs (stream-K): 16384 bytes of per-tile arrival counters, then FP32
+ * partial sums, 0 when the tiles fill whole waves; plus, when K % 8 != 0
+ * (per channel), a copy of x with rows padded to a multiple of 8 elements
+ * (a TMA tensor's rows must be multiples of 16 bytes) after the counters
+ * and partial sums, rewritten by every call.  Like the GEMV workspace it
+ * must be zero-filled before its first use, and every tf_gemm that
+ * completes leaves its counters at zero.  After a call that reported a
+ * device error (tf_device_error nonzero) zero it again before reusing it.
  */
 int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
@@ -250,6 +262,12 @@ int tf_gemm_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  * With K % 8 != 0 (per channel) the workspace is required (it holds the
  * padded copy of x, made by a small kernel on the stream before the GEMM);
  * NULL gives TF_ERR_WORKSPACE.
+ * M <= 8 with K % 8 == 0 is a weight stream, not a contraction: it runs on
+ * the slab or tile GEMV of tf_gemv (every weight dequantised to BF16 in
+ * registers, exactly as here, and fed to mma.sync), given the workspace
+ * that tf_gemm_workspace_size asks for, or with none when that is 0; with
+ * workspace NULL on a layer that needs one, the tensor-core pipeline runs
+ * with every tile whole.
  */
 int tf_gemm(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,
             const uint16_t* x, uint16_t* y, int M, void* workspace, size_t workspace_bytes,

@@ -4,9 +4,10 @@ word, writes nothing and exits with no copy in flight.
 
 The test hook tf_test_stall_copies makes the producers issue no copies, so
 that the first wait of each kernel family runs out after 1 ms: the stream
-GEMV (0x700), the tile and slab GEMVs (0x600) and the GEMM (one of its role
-codes 0x100..0x500).  The next call, with the hook off, must be correct and
-report no error: the context is intact and no workspace was left dirty.
+GEMV (0x700), the tile and slab GEMVs (0x600, also behind tf_gemm at
+M <= 8) and the GEMM (one of its role codes 0x100..0x500).  The next call,
+with the hook off, must be correct and report no error: the context is
+intact and no workspace was left dirty.
 """
 
 import time
@@ -42,6 +43,7 @@ CASES = [
     ("gemv_noalloc", 1024, 2048, 4, 128, 1, {0x600}),   # tile GEMV on the fixed scratch array
     ("gemm", 4096, 4096, 4, 128, 256, {0x100, 0x200, 0x300, 0x400, 0x500}),
     ("gemm", 2048, 1024, 8, 0, 64, {0x100, 0x200, 0x300, 0x400, 0x500}),
+    ("gemm", 2048, 1024, 8, 0, 4, {0x600}),             # M <= 8: tf_gemm on the tile GEMV
 ]
 
 

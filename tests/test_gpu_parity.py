@@ -103,22 +103,81 @@ def test_gemv_deterministic_and_workspace_reusable():
     for _ in range(3):
         b = to_host_bits(tf.gemv(W, x))
         np.testing.assert_array_equal(a, b)
-    # the workspace is handed back zero-filled (counters reset)
+    # the counters (first 16 KB of the workspace) are handed back at zero
     ws = W.workspace(1)
     import torch
-    assert ws.numel() > 16
-    n_counter = N // 128 * 8
-    assert int(ws.view(torch.int32)[-((n_counter + 63) // 64 * 64):].abs().sum()) == 0
+    assert ws.numel() > 16384
+    assert int(ws[:16384].view(torch.int32).abs().sum()) == 0
 
 
 @pytest.mark.parametrize("N,K,bits,group", FORMATS)
-@pytest.mark.parametrize("M", [1, 16, 37])
+@pytest.mark.parametrize("M", [1, 9, 16, 37, 64])
 def test_gemm_small(N, K, bits, group, M):
+    """tf_gemm with its workspace (M <= 8 on these layers: the tile GEMV;
+    above: the tensor-memory pipeline with K-split tiles) and without one
+    (every tile whole in the tensor-memory pipeline), both against the
+    oracle."""
     qw, W = layer(N, K, bits, group, 31)
     xb = synth.make_activations(M, K, 31, outliers=True)
-    y = to_host_bits(tf.gemm(W, to_dev_bf16(xb)))
+    x = to_dev_bf16(xb)
     ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
-    check_close(y, ref, f"gemm {N}x{K} w{bits} g{group} M={M}")
+    check_close(to_host_bits(tf.gemm(W, x)), ref, f"gemm {N}x{K} w{bits} g{group} M={M}")
+    check_close(to_host_bits(tf.gemm(W, x, stream_k=False)), ref, f"tcgen05 gemm {N}x{K} w{bits} g{group} M={M}")
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", [(3000, 4096, 4, 128, 40), (1000, 8192, 8, 0, 64), (2440, 1536, 4, 64, 9),
+                                              (1024, 11008, 4, 128, 4)])
+def test_gemm_few_tokens_deterministic(N, K, bits, group, M):
+    """Few tokens: K is split across CTAs (tensor-memory stream-K, or the tile
+    GEMV at M <= 8) and the partial sums are added in a fixed order: the same
+    bits every run."""
+    qw, W = layer(N, K, bits, group, 36)
+    xb = synth.make_activations(M, K, 36)
+    x = to_dev_bf16(xb)
+    assert tf.gemm_workspace_size(N, K, bits, group, M) > 0
+    a = to_host_bits(tf.gemm(W, x))
+    check_close(a, tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb), f"gemm M={M}")
+    for _ in range(2):
+        np.testing.assert_array_equal(a, to_host_bits(tf.gemm(W, x)))
+
+
+def test_gemm_few_tokens_on_the_slab_gemv():
+    """M <= 8 on a layer with a 16-row slab per SM: tf_gemm runs the slab GEMV
+    (per-weight BF16 rounding, no workspace), with or without a workspace."""
+    N, K, M = 4096, 2048, 8
+    qw, W = layer(N, K, 4, 128, 37)
+    assert tf.gemm_workspace_size(N, K, 4, 128, M) == 0
+    xb = synth.make_activations(M, K, 37)
+    x = to_dev_bf16(xb)
+    ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, 4, 128, K, xb)
+    a = to_host_bits(tf.gemm(W, x))
+    check_close(a, ref, "gemm M=8 slab GEMV")
+    np.testing.assert_array_equal(a, to_host_bits(tf.gemm(W, x, stream_k=False)))
+
+
+def test_one_workspace_serves_every_layer():
+    """Split-K workspaces keep their arrival counters in a fixed region at the
+    start, so one zeroed workspace, as large as the largest need, can serve
+    layers of any shape in turn: tile GEMV calls (through tf_gemv and
+    tf_gemm) and tensor-memory stream-K calls alternate on it and give the
+    bits of private workspaces."""
+    import torch
+    calls = [(tf.gemv, (1024, 2048, 4, 128), 1), (tf.gemm, (2048, 1024, 8, 0), 4),
+             (tf.gemm, (20480, 384, 4, 128), 80), (tf.gemv, (640, 4096, 8, 64), 5), (tf.gemm, (1000, 8192, 4, 64), 64)]
+    sizes = [(tf.gemv_workspace_size if fn is tf.gemv else tf.gemm_workspace_size)(*shape, M) for fn, shape, M in calls]
+    assert all(n > 0 for n in sizes)
+    shared = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
+    layers, want = [], []
+    for i, (fn, shape, M) in enumerate(calls):
+        _, W = layer(*shape, 40 + i)
+        x = to_dev_bf16(synth.make_activations(M, shape[1], 40 + i))
+        layers.append((fn, W, x))
+        want.append(to_host_bits(fn(W, x)))  # its own cached workspace
+    for _ in range(3):
+        for (fn, W, x), w in zip(layers, want):
+            np.testing.assert_array_equal(to_host_bits(fn(W, x, workspace=shared)), w)
+    torch.cuda.synchronize()
+    assert int(shared[:16384].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
 
 
 @pytest.mark.parametrize("M", [128, 200, 256, 300, 640])
@@ -175,14 +234,15 @@ def test_gemv_slab_long_k(N, K, bits, group, M):
     check_close(y[:, rows], ref, f"long-K slab gemv {N}x{K} w{bits} g{group} M={M}")
 
 
-# Shapes whose tiles the GEMM splits along K on a 152-SM GB300: a partial wave
-# over more than one wave of tiles (N = 20480 and 19712 rows, a ragged
-# N = 20000 with a ragged K), and every tile split when there are few tiles
-# (M = 37 over 3 tiles; M = 1 over 2 tiles with 32 k-iterations each, so
-# 32 CTAs add into one tile).
+# Shapes whose tiles the tensor-memory GEMM splits along K on a 152-SM GB300
+# (M > 8, or per-channel layers with K % 8 != 0, which the GEMV kernels do
+# not take): a partial wave over more than one wave of tiles (N = 20480 and
+# 19712 rows, a ragged N = 20000 with K % 8 != 0), and every tile split when
+# there are few tiles (M = 100 over 3 tiles; M = 1 over 2 tiles of 33
+# k-iterations, four CTAs adding into each).
 STREAM_K = [
-    (20480, 384, 4, 128, 16), (19712, 2048, 4, 128, 300), (20000, 1016, 4, 0, 40),
-    (384, 4096, 8, 64, 37), (256, 4096, 8, 0, 1), (2048, 1536, 4, 128, 512),
+    (20480, 384, 4, 128, 80), (19712, 2048, 4, 128, 300), (20000, 1017, 4, 0, 40),
+    (384, 8192, 8, 64, 100), (256, 4097, 8, 0, 1), (2048, 1536, 4, 128, 512),
 ]
 
 
@@ -198,9 +258,10 @@ def test_gemm_stream_k_and_whole_tiles(N, K, bits, group, M):
     x = to_dev_bf16(xb)
     ref = tf_oracle.reference(qw.qweight, qw.scales, qw.zeros, bits, group, K, xb)
     y_sk = to_host_bits(tf.gemm(W, x))
-    y_dp = to_host_bits(tf.gemm(W, x, stream_k=False))
     check_close(y_sk, ref, f"stream-K gemm {N}x{K} M={M}")
-    check_close(y_dp, ref, f"whole-tile gemm {N}x{K} M={M}")
+    if K % 8 == 0:  # else the padded copy of x needs the workspace (whole tiles are not available)
+        y_dp = to_host_bits(tf.gemm(W, x, stream_k=False))
+        check_close(y_dp, ref, f"whole-tile gemm {N}x{K} M={M}")
     np.testing.assert_array_equal(y_sk, to_host_bits(tf.gemm(W, x)))  # same sums every run
     assert tf.device_error() == 0
 
