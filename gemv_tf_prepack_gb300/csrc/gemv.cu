@@ -9,13 +9,14 @@
 // fragments go straight into mma.sync so that the tensor cores do the
 // multiply-accumulate instead of CUDA-core FMAs.
 //
-// The layers with at least one 16-row slab per SM and groups of 64, any
-// multiple of 128 or per channel (every decode projection of a Llama-class
-// model) go to the stream GEMV of gemv_stream.cu, which skips the per-weight
-// BF16 rounding.  This file holds the entry points, the routing, and the two
-// GEMVs for the other layers, which dequantise each weight to BF16 in
-// registers (bit-exact, as tf_dequant) and share one inner step (one 16-row
-// x 128-column unit per warp):
+// The layers with groups of 64, any multiple of 128 or per channel whose
+// activations fit in shared memory (every decode projection of a
+// Llama-class model) go to the stream GEMV of gemv_stream.cu, which skips
+// the per-weight BF16 rounding.  This file holds the entry points, the
+// routing, and the two GEMVs for the other layers (groups of 32, or
+// activations too large), and for tf_gemm at M <= 8, which dequantise each
+// weight to BF16 in registers (bit-exact, as tf_dequant) and share one inner
+// step (one 16-row x 128-column unit per warp):
 //  * slab GEMV, for groups of 32 on layers with at least as many 16-row slabs
 //    as SMs whose activations fit in shared memory: each CTA owns whole slabs
 //    over all of K, its eight (or sixteen) warps split K, and a slab's partial

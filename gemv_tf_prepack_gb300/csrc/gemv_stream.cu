@@ -1,6 +1,6 @@
-// Stream GEMV of libtf: token generation (M <= 8) for layers with at least
-// one 16-row slab per SM, INT4 or INT8 codes, groups of 64, any multiple of
-// 128, or per channel.
+// Stream GEMV of libtf: token generation (M <= 8) for layers with INT4 or
+// INT8 codes, groups of 64, any multiple of 128, or per channel, whose
+// activations fit in shared memory next to the weight ring.
 //
 // TileFuse, Methodology 3 ("GEMV dataflow co-design"): at batch 1 a
 // quantised linear layer stops being bound by memory once unpacking and
@@ -28,11 +28,14 @@
 //    bit); the pages' "dequantise to BF16" becomes "codes exact in FP16, scale
 //    and zero in FP32".
 //
-// Work split.  Each CTA (one per SM) owns whole 16-row slabs, the slab count
-// shared out as evenly as whole slabs allow (the CTAs that start first take
-// the extra ones); a slab split between two CTAs
-// would need a cross-SM reduction whose L2 round trip at the end of the
-// layer costs more than the up-to-one-slab imbalance.  The CTA's slabs are
+// Work split.  Each CTA (one per SM, or one per slab on layers with fewer
+// 16-row slabs than SMs) owns whole slabs, the slab count shared out as
+// evenly as whole slabs allow (the CTAs that start first take the extra
+// ones); a slab split between two CTAs would need a cross-SM reduction
+// whose L2 round trip at the end of the layer costs more than the
+// up-to-one-slab imbalance.  Even a layer of a few slabs runs faster this
+// way than with K split across all SMs (the tile GEMV of gemv.cu: 2 to 5
+// times slower on 256 to 2304-row layers).  The CTA's slabs are
 // one contiguous byte range of the blob (units are slab-major), shared out
 // evenly over its sixteen warps: a warp's share is a contiguous run of
 // units, which it streams through its own small ring of shared-memory stages
@@ -627,10 +630,7 @@ int stream_plan(const Geometry& G, int M, StreamPlan* P) {
   const int sms = sm_count();
   if (sms <= 0) return 0;
   const int nslab = (G.N + kSlabN - 1) / kSlabN;
-  // K % 8 != 0 (per channel only): the other GEMVs move x rows as 16-byte
-  // pieces, so this kernel takes every such layer, on fewer CTAs than SMs
-  // when the layer has fewer slabs
-  if (nslab < sms && G.K % 8 == 0) return 0;
+  // one CTA per slab on layers with fewer slabs than SMs
   StreamPlan S{};
   S.G = nslab < sms ? nslab : sms;
   S.Mp = M == 1 ? 1 : (M + 1) / 2 * 2;

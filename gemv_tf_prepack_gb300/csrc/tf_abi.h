@@ -78,8 +78,8 @@ inline int check_epi(const Epi& e) {
   return TF_OK;
 }
 
-// The stream GEMV (gemv_stream.cu): M <= 8, at least one 16-row slab per
-// SM, groups of 64, any multiple of 128 or per channel; no workspace.
+// The stream GEMV (gemv_stream.cu): M <= 8, groups of 64, any multiple of
+// 128 or per channel, activations that fit in shared memory; no workspace.
 // stream_plan returns 1 and fills *P when it takes the layer.
 struct StreamPlan {
   int G, Mp, NS, npre, off_x, off_xs, off_red, off_ctl, max_slabs, half, compact;

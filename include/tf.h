@@ -179,8 +179,7 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
 /*
  * Workspace bytes tf_gemv needs on the current device for this layer and M
  * (16384 bytes of per-block arrival counters, then the split-K partial
- * sums; 0 for layers with at least one 16-row slab per SM, whose blocks
- * each stream whole slabs).  The workspace must be zero-filled before its
+ * sums; 0 for the layers whose blocks each stream whole slabs).  The workspace must be zero-filled before its
  * first use; every tf_gemv that completes leaves the arrival counters at
  * zero again (the partial sums are always written before they are read), so
  * one workspace can be reused by calls ordered on one stream, for any layer
@@ -196,26 +195,28 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  * Each weight code is read from HBM once, unpacked in registers and fed
  * straight to the tensor cores (mma.sync, FP32 accumulation), with the whole
  * chip streaming weights.
- *  - Layers with at least one 16-row slab per SM and groups of 64, multiples
- *    of 128 or per channel: every block owns whole slabs, each warp streams
- *    a contiguous run of them.  The codes enter the tensor cores exactly (as
+ *  - Groups of 64, multiples of 128 or per channel, with x small enough to
+ *    stay resident in shared memory (M * K up to about 64K elements): every
+ *    block (one per SM, or one per 16-row slab on smaller layers) owns whole
+ *    slabs, each warp streams a contiguous run of them.  The codes enter the tensor cores exactly (as
  *    FP16), x is converted to FP16 with a power-of-two scale per 128-column
  *    block (exact), and (q - z) * s is applied per group in FP32 to the
  *    sums: the result is sum_k x * (q - z) * s without rounding each
  *    dequantised weight to BF16 (tf_dequant and tf_gemm keep that rounding).
- *  - Groups of 32 on such layers: whole slabs per block, K split over the
- *    block's warps, each weight dequantised to BF16 in registers as above.
- *  - The others (few rows, or x too large to stay resident): K split across
- *    all blocks, the last-arriving block of each row block adding the
- *    partial sums.
+ *  - The others (groups of 32, or x too large for the above) on layers with
+ *    at least one 16-row slab per SM and K >= 1024, x resident: whole slabs
+ *    per block, K split over the block's warps, each weight dequantised to
+ *    BF16 in registers (as tf_dequant and tf_gemm do).
+ *  - The rest: K split across all blocks, the last-arriving block of each
+ *    row block adding the partial sums.
  * Every addition happens in a fixed order, so results are deterministic run
  * to run.
  * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),
  * y [M, N] BF16, workspace (16-byte aligned, >= tf_gemv_workspace_size; may
  * be NULL when that is 0).  1 <= M <= 8, else TF_ERR_UNSUPPORTED.  With
- * K % 8 != 0 (per channel) the stream GEMV takes the layer whatever its N,
- * reading x element by element; its activations must fit in shared memory
- * next to the weight ring (M * K up to about 64K elements), else
+ * K % 8 != 0 (per channel) only the stream GEMV takes the layer, reading x
+ * element by element: its activations must fit in shared memory next to
+ * the weight ring (M * K up to about 64K elements), else
  * TF_ERR_UNSUPPORTED.
  */
 int tf_gemv(const void* blob, size_t blob_bytes, int N, int K, int bits, int group,

@@ -95,9 +95,9 @@ def test_gemv_slab_deterministic():
 
 
 def test_gemv_deterministic_and_workspace_reusable():
-    """Tile GEMV with K split over many CTAs (1024 rows: fewer slabs than SMs)."""
+    """Tile GEMV with K split over many CTAs (1024 rows, groups of 32)."""
     N, K = 1024, 11008
-    qw, W = layer(N, K, 4, 128, 4)
+    qw, W = layer(N, K, 4, 32, 4)
     x = to_dev_bf16(synth.make_activations(1, K, 4))
     a = to_host_bits(tf.gemv(W, x))
     for _ in range(3):
@@ -162,8 +162,8 @@ def test_one_workspace_serves_every_layer():
     tf_gemm) and tensor-memory stream-K calls alternate on it and give the
     bits of private workspaces."""
     import torch
-    calls = [(tf.gemv, (1024, 2048, 4, 128), 1), (tf.gemm, (2048, 1024, 8, 0), 4),
-             (tf.gemm, (20480, 384, 4, 128), 80), (tf.gemv, (640, 4096, 8, 64), 5), (tf.gemm, (1000, 8192, 4, 64), 64)]
+    calls = [(tf.gemv, (1024, 2048, 4, 32), 1), (tf.gemm, (2048, 1024, 8, 0), 4),
+             (tf.gemm, (20480, 384, 4, 128), 80), (tf.gemv, (640, 4096, 8, 32), 5), (tf.gemm, (1000, 8192, 4, 64), 64)]
     sizes = [(tf.gemv_workspace_size if fn is tf.gemv else tf.gemm_workspace_size)(*shape, M) for fn, shape, M in calls]
     assert all(n > 0 for n in sizes)
     shared = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
@@ -327,7 +327,8 @@ def test_awq_import_parity(N, K, group):
 # element stores (N % 8 != 0) and the GEMM stream-K fixup.
 BIAS_CASES = [
     (2440, 1152, 4, 128, 1, "gemv"), (2440, 1152, 8, 0, 3, "gemv"), (200, 192, 4, 64, 8, "gemv"),
-    (1000, 1016, 4, 0, 1, "gemv"), (384, 4096, 8, 64, 37, "gemm"), (20000, 1016, 4, 0, 40, "gemm"),
+    (1000, 1016, 4, 0, 1, "gemv"), (200, 192, 4, 32, 8, "gemv"),  # the last one: tile GEMV
+    (384, 4096, 8, 64, 37, "gemm"), (20000, 1016, 4, 0, 40, "gemm"),
     (2048, 1536, 4, 128, 512, "gemm"), (1004, 1016, 4, 0, 300, "gemm"),
 ]
 
@@ -372,7 +373,8 @@ def test_symmetric_zero_point(N, K, bits, group):
 # layers have the same number of units, so the blob sizes agree and only the
 # header can tell them apart.
 HEADER_CASES = [
-    ("gemv", (1024, 2048, 4, 128), (2048, 1024), 1),   # tile GEMV (fewer slabs than SMs)
+    ("gemv", (1024, 2048, 4, 128), (2048, 1024), 1),   # stream GEMV, one CTA per slab
+    ("gemv", (1024, 2048, 4, 32), (2048, 1024), 1),    # tile GEMV (groups of 32, fewer slabs than SMs)
     ("gemv", (4096, 2048, 4, 32), (2048, 4096), 1),    # slab GEMV (groups of 32)
     ("gemm", (4096, 11008, 4, 128), (11008, 4096), 64),
     ("gemm", (4096, 11008, 4, 128), (11008, 4096), 300),
@@ -381,7 +383,7 @@ HEADER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("call,desc,other,M", HEADER_CASES, ids=[f"{c[0]}-{c[1][0]}x{c[1][1]}-M{c[3]}" for c in HEADER_CASES])
+@pytest.mark.parametrize("call,desc,other,M", HEADER_CASES, ids=[f"{c[0]}-{c[1][0]}x{c[1][1]}g{c[1][3]}-M{c[3]}" for c in HEADER_CASES])
 def test_mismatched_header_rejected_on_device(call, desc, other, M):
     """A device blob of another layer with the same size: the kernel reads its
     header, records 0x800 in the device error word and writes nothing (y and

@@ -1,5 +1,6 @@
-"""The stream GEMV (M <= 8, layers with at least one 16-row slab per SM, groups
-of 64, multiples of 128 or per channel) against the float64 oracle.
+"""The stream GEMV (M <= 8, groups of 64, multiples of 128 or per channel,
+activations that fit in shared memory; one CTA per SM, or per 16-row slab on
+smaller layers) against the float64 oracle.
 
 Its arithmetic differs from the other kernels' (codes exact as FP16
 subnormals, activations scaled per token by a power of two, scale and zero
@@ -37,8 +38,9 @@ def _sms():
 
 
 def _is_stream(N, K, bits, group, M):
-    """The routing rule: at least one slab per SM, groups other than 32, M <= 8, no workspace."""
-    return -(-N // 16) >= _sms() and group != 32 and M <= 8 and tf.gemv_workspace_size(N, K, bits, group, M) == 0
+    """The routing rule: groups other than 32, M <= 8, activations of at most
+    64K elements, no workspace."""
+    return group != 32 and M <= 8 and M * K <= 65536 and tf.gemv_workspace_size(N, K, bits, group, M) == 0
 
 
 STREAM_FORMATS = [
@@ -46,6 +48,9 @@ STREAM_FORMATS = [
     (2560, 1280, 8, 64), (5000, 3072, 4, 128), (2450, 384, 4, 128), (2448, 1024, 4, 256),
     (2447, 520, 4, 0), (2500, 640, 8, 128), (2433, 136, 8, 0), (4104, 8192, 4, 128),
     (2600, 8192, 8, 0), (2440, 8192, 4, 64),  # M = 8: activations of 128 KB, half-size ring stages
+    # fewer 16-row slabs than SMs: one CTA per slab
+    (1024, 4096, 4, 128), (256, 512, 4, 128), (136, 200, 8, 0), (1000, 1016, 4, 0), (8, 8, 4, 0),
+    (2048, 4096, 8, 64), (130, 256, 8, 128), (2431, 1024, 4, 128),
 ]
 
 
