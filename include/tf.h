@@ -203,12 +203,13 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  *    block (exact), and (q - z) * s is applied per group in FP32 to the
  *    sums: the result is sum_k x * (q - z) * s without rounding each
  *    dequantised weight to BF16 (tf_dequant and tf_gemm keep that rounding).
- *  - The others (groups of 32, or x too large for the above) on layers with
- *    at least one 16-row slab per SM and K >= 1024, x resident: whole slabs
- *    per block, K split over the block's warps, each weight dequantised to
+ *  - The others (groups of 32, or x too large for the above) with K >= 1024
+ *    and x resident: whole slabs per block (one block per slab on small
+ *    layers), K split over the block's warps, each weight dequantised to
  *    BF16 in registers (as tf_dequant and tf_gemm do).
- *  - The rest: K split across all blocks, the last-arriving block of each
- *    row block adding the partial sums.
+ *  - The rest (K < 1024, or x too large even for that): K split across all
+ *    blocks, the last-arriving block of each row block adding the partial
+ *    sums.
  * Every addition happens in a fixed order, so results are deterministic run
  * to run.
  * Device pointers: blob (16-byte aligned), x [M, K] BF16 (16-byte aligned),

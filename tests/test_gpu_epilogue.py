@@ -47,7 +47,7 @@ GATE_CASES = [
     (2056, 8192, 4, 128, 8, "gemv"),   # M = 8 on a long K: half-size ring stages
     (4096, 1024, 4, 128, 1, "gemv"),   # 512 slabs: compact parking of the sums
     (96, 1024, 4, 128, 1, "gemv"),     # stream GEMV, one CTA per slab
-    (96, 1024, 4, 32, 1, "gemv"), (96, 4096, 8, 32, 5, "gemv"),  # tile GEMV: split-K last arriver
+    (96, 896, 4, 32, 1, "gemv"), (96, 768, 8, 32, 5, "gemv"),  # tile GEMV (K < 1024): split-K last arriver
     (1224, 1024, 4, 32, 2, "gemv"),    # slab GEMV (groups of 32)
     (1024, 1024, 4, 128, 37, "gemm"), (1024, 2048, 8, 64, 300, "gemm"), (200, 1024, 4, 0, 1, "gemm"),
 ]
@@ -107,7 +107,7 @@ def test_silu_gate_deterministic_and_output_only():
 QKV_CASES = [
     (2440, 1024, 4, 128, 1, "gemv", 1000, 720), (3072, 2048, 8, 0, 4, "gemv", 2048, 512),
     (4104, 8192, 4, 64, 8, "gemv", 4096, 0), (384, 1024, 4, 128, 2, "gemv", 128, 128),
-    (384, 1024, 4, 32, 2, "gemv", 128, 128),  # tile GEMV
+    (384, 896, 4, 32, 2, "gemv", 128, 128),  # tile GEMV (K < 1024)
     (2440, 1024, 4, 32, 1, "gemv", 2, 2000), (1536, 2048, 4, 128, 33, "gemm", 1024, 257),
     (3000, 1024, 8, 128, 300, "gemm", 1500, 500), (1004, 1016, 4, 0, 17, "gemm", 1, 1),
 ]

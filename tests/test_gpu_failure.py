@@ -39,12 +39,13 @@ CASES = [
     ("gemv", 4096, 4096, 4, 128, 1, {0x700}),           # stream GEMV
     ("gemv", 3000, 2048, 8, 0, 3, {0x700}),
     ("gemv", 1024, 2048, 4, 128, 1, {0x700}),           # stream GEMV, one CTA per slab
-    ("gemv", 1024, 2048, 4, 32, 1, {0x600}),            # tile GEMV (groups of 32, fewer slabs than SMs)
+    ("gemv", 1024, 768, 4, 32, 1, {0x600}),             # tile GEMV (K < 1024)
     ("gemv", 4096, 2048, 4, 32, 1, {0x600}),            # slab GEMV (groups of 32)
-    ("gemv_noalloc", 1024, 2048, 4, 32, 1, {0x600}),    # tile GEMV on the fixed scratch array
+    ("gemv_noalloc", 1024, 768, 4, 32, 1, {0x600}),     # tile GEMV on the fixed scratch array
     ("gemm", 4096, 4096, 4, 128, 256, {0x100, 0x200, 0x300, 0x400, 0x500}),
     ("gemm", 2048, 1024, 8, 0, 64, {0x100, 0x200, 0x300, 0x400, 0x500}),
-    ("gemm", 2048, 1024, 8, 0, 4, {0x600}),             # M <= 8: tf_gemm on the tile GEMV
+    ("gemm", 2048, 1024, 8, 0, 4, {0x600}),             # M <= 8: tf_gemm on the slab GEMV
+    ("gemm", 2048, 768, 8, 0, 4, {0x600}),              # and on the tile GEMV (K < 1024)
 ]
 
 
