@@ -46,6 +46,9 @@ BITS, GROUP = 4, 128
 SQUARE = [("w8_per_channel", 8192, 8192, 8, 0, 5, (1, 8, 64)), ("w4_g64", 8192, 8192, 4, 64, 6, (1, 8, 64))]
 LARGE = [("32768x8192", 32768, 8192, 4, 128, 10, (1,)), ("8192x32768", 8192, 32768, 4, 128, 11, (1,)),
          ("32768x32768", 32768, 32768, 4, 128, 12, (1,))]
+# layers with fewer 16-row slabs than SMs (GQA-style K/V projections and the like)
+SMALL = [("1024x11008_w4g128", 1024, 11008, 4, 128, 13, (1, 4)), ("2048x4096_w8", 2048, 4096, 8, 0, 14, (1, 8)),
+         ("1024x11008_w4g32", 1024, 11008, 4, 32, 15, (1,))]
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -272,12 +275,13 @@ def time_launches(torch, fn, Ws, x, y, stream):
 
 
 def extra_layers(torch, tf, synth, stream, hbm_peak, peak_src):
-    """The square 8192^2 layers (W8 per channel, W4 g64) at M = 1, 8, 64 and
-    the large W4 g128 layers at M = 1: us per launch, GB/s of algorithmic
-    bytes and the fraction of the measured HBM copy bandwidth (all of these
-    are bound by HBM: flop/byte <= 224 at M = 64)."""
+    """The square 8192^2 layers (W8 per channel, W4 g64) at M = 1, 8, 64, the
+    large W4 g128 layers at M = 1 and layers with fewer 16-row slabs than SMs:
+    us per launch, GB/s of algorithmic bytes and the fraction of the measured
+    HBM copy bandwidth (all of these are bound by HBM: flop/byte <= 224 at
+    M = 64)."""
     out = {}
-    for group_name, cases in (("square_8192", SQUARE), ("large_m1", LARGE)):
+    for group_name, cases in (("square_8192", SQUARE), ("large_m1", LARGE), ("small_n", SMALL)):
         res = {}
         for name, N, K, bits, group, seed, Ms in cases:
             qw = synth.make_weights(N, K, bits, group, seed)
