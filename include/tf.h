@@ -66,10 +66,12 @@
 extern "C" {
 #endif
 
-#define TF_VERSION 5  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias; 4: tf_gemv_noalloc,
+#define TF_VERSION 6  /* 3: tf_prepack_awq, tf_gemv_bias, tf_gemm_bias; 4: tf_gemv_noalloc,
                          TF_ERR_SCRATCH_LIMIT, device-side check of the blob header;
                          5: tf_prepack_gate_up, tf_gemv_silu_gate, tf_gemm_silu_gate,
-                         tf_gemv_qkv, tf_gemm_qkv */
+                         tf_gemv_qkv, tf_gemm_qkv; 6: workspaces with a fixed leading
+                         counter region (one workspace serves every layer), tf_gemm
+                         at M <= 8 on the GEMV kernels */
 
 #define TF_OK 0
 #define TF_ERR_INVALID_ARG (-1) /* null pointer, bad size or bad combination */

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol():
     lib = tf.lib()
     for d in decl:
         getattr(lib, d)
-    assert tf.version() == 5
+    assert tf.version() == 6
 
 
 @pytest.mark.parametrize("N,K,bits,group", [
