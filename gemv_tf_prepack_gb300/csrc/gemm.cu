@@ -466,9 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     int ps = 0;
     uint32_t pph = 0;
     unsigned slab = (unsigned)h;  // this warp's slabs are h, h + 2, h + 4, ... of the CTA's stream
-    // A stage's proxy fence and full-barrier arrive are deferred until the
-    // next k-step's tile has been unpacked and dequantised, so that the
-    // fence's wait for the stores overlaps that work.
+    // With more than 64 tokens, a stage's proxy fence and full-barrier
+    // arrive are deferred until the next k-step's tile has been unpacked and
+    // dequantised, so that the fence's wait for the stores overlaps that
+    // work.
     int pend = -1;
     bool ok = true;
     Sched sc = sched_begin(a);
@@ -523,7 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         *reinterpret_cast<uint4*>(wsl + dst[0][1]) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         *reinterpret_cast<uint4*>(wsl + dst[1][0]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(wsl + dst[1][1]) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        pend = (int)os;
+        if (a.BN <= 64) {
+          // few tokens: the MMAs are waiting for this stage, publish it now
+          // (2-3 % faster at M = 16-64; the deferral below pays only at large M)
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.full_op + 8 * os);
+        } else {
+          pend = (int)os;
+        }
         slab += 2;
       }
     }
