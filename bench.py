@@ -44,8 +44,8 @@ PREFILL_M = 2048
 BITS, GROUP = 4, 128
 # (name, N, K, bits, group, seed, M list): square layers and the large-dimension layers
 SQUARE = [("w8_per_channel", 8192, 8192, 8, 0, 5, (1, 8, 64)), ("w4_g64", 8192, 8192, 4, 64, 6, (1, 8, 64))]
-LARGE = [("32768x8192", 32768, 8192, 4, 128, 10, (1,)), ("8192x32768", 8192, 32768, 4, 128, 11, (1,)),
-         ("32768x32768", 32768, 32768, 4, 128, 12, (1,))]
+LARGE = [("32768x8192", 32768, 8192, 4, 128, 10, (1, 4096)), ("8192x32768", 8192, 32768, 4, 128, 11, (1, 4096)),
+         ("32768x32768", 32768, 32768, 4, 128, 12, (1, 4096))]
 # layers with fewer 16-row slabs than SMs (GQA-style K/V projections and the like)
 SMALL = [("1024x11008_w4g128", 1024, 11008, 4, 128, 13, (1, 4)), ("2048x4096_w8", 2048, 4096, 8, 0, 14, (1, 8)),
          ("1024x11008_w4g32", 1024, 11008, 4, 32, 15, (1,))]
@@ -274,14 +274,15 @@ def time_launches(torch, fn, Ws, x, y, stream):
     return e0.elapsed_time(e1) * 1e3 / (reps * len(Ws))
 
 
-def extra_layers(torch, tf, synth, stream, hbm_peak, peak_src):
+def extra_layers(torch, tf, synth, stream, hbm_peak, tc_peak, peak_src):
     """The square 8192^2 layers (W8 per channel, W4 g64) at M = 1, 8, 64, the
-    large W4 g128 layers at M = 1 and layers with fewer 16-row slabs than SMs:
-    us per launch, GB/s of algorithmic bytes and the fraction of the measured
-    HBM copy bandwidth (all of these are bound by HBM: flop/byte <= 224 at
-    M = 64)."""
+    large W4 g128 layers at M = 1 and 4096, and layers with fewer 16-row slabs
+    than SMs: us per launch, GB/s of algorithmic bytes, TFLOP/s, and the
+    fraction of the measured peak that bounds the launch (HBM copy bandwidth
+    up to M = 64, where flop/byte <= 224; the burst BF16 tensor peak at
+    M = 4096)."""
     out = {}
-    for group_name, cases in (("square_8192", SQUARE), ("large_m1", LARGE), ("small_n", SMALL)):
+    for group_name, cases in (("square_8192", SQUARE), ("large", LARGE), ("small_n", SMALL)):
         res = {}
         for name, N, K, bits, group, seed, Ms in cases:
             qw = synth.make_weights(N, K, bits, group, seed)
@@ -299,12 +300,16 @@ def extra_layers(torch, tf, synth, stream, hbm_peak, peak_src):
 
                 us = time_launches(torch, fn, Ws, x, y, stream)
                 gbs = algo_bytes(M, N, K, bits, group) / (us * 1e-6) / 1e9
+                tfs = 2.0 * M * N * K / us / 1e6
+                tensor = M > 64
                 res[f"{name}_M{M}"] = {"call": call.__name__, "us": round(us, 2), "GB/s": round(gbs, 1),
-                                       "frac": round(gbs / hbm_peak, 4), "TFLOP/s": round(2.0 * M * N * K / us / 1e6, 2)}
+                                       "TFLOP/s": round(tfs, 2), "bound": "tensor" if tensor else "hbm",
+                                       "frac": round(tfs / tc_peak if tensor else gbs / hbm_peak, 4)}
+                del x, y
             del Ws
             torch.cuda.empty_cache()
         out[group_name] = res
-    out["peak"] = {"hbm_gbs": hbm_peak, "source": peak_src}
+    out["peak"] = {"hbm_gbs": hbm_peak, "bf16_tflops": tc_peak, "source": peak_src}
     out["l2"] = "each layer rotates through weight copies totalling more than 3x L2; one CUDA graph per layer"
     return out
 
@@ -489,7 +494,7 @@ def run_ours(args, rank, world):
         L["Ws"].clear(); L["xs"].clear(); L["ys"].clear()
     del psingles, pbig, piso
     torch.cuda.empty_cache()
-    extras = None if args.no_extras else extra_layers(torch, tf, synth, stream, hbm_peak, peak_src)
+    extras = None if args.no_extras else extra_layers(torch, tf, synth, stream, hbm_peak, tc_peak, peak_src)
 
     err = tf.device_error()
     if rank != 0:
