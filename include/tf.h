@@ -181,13 +181,13 @@ int tf_dequant(const void* blob, size_t blob_bytes, int N, int K, int bits, int 
 /*
  * Workspace bytes tf_gemv needs on the current device for this layer and M
  * (16384 bytes of per-block arrival counters, then the split-K partial
- * sums; 0 for the layers whose blocks each stream whole slabs).  The workspace must be zero-filled before its
- * first use; every tf_gemv that completes leaves the arrival counters at
- * zero again (the partial sums are always written before they are read), so
- * one workspace can be reused by calls ordered on one stream, for any layer
- * (see the workspace rule above).  After a call that reported a device
- * error (tf_device_error nonzero) zero the workspace again before reusing
- * it.
+ * sums; 0 for the layers whose blocks each stream whole slabs).  The
+ * workspace must be zero-filled before its first use; every tf_gemv that
+ * completes leaves the arrival counters at zero again (the partial sums are
+ * always written before they are read), so one workspace can be reused by
+ * calls ordered on one stream, for any layer (see the workspace rule
+ * above).  After a call that reported a device error (tf_device_error
+ * nonzero) zero the workspace again before reusing it.
  */
 int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* bytes);
 
@@ -200,11 +200,12 @@ int tf_gemv_workspace_size(int N, int K, int bits, int group, int M, size_t* byt
  *  - Groups of 64, multiples of 128 or per channel, with x small enough to
  *    stay resident in shared memory (M * K up to about 64K elements): every
  *    block (one per SM, or one per 16-row slab on smaller layers) owns whole
- *    slabs, each warp streams a contiguous run of them.  The codes enter the tensor cores exactly (as
- *    FP16), x is converted to FP16 with a power-of-two scale per 128-column
- *    block (exact), and (q - z) * s is applied per group in FP32 to the
- *    sums: the result is sum_k x * (q - z) * s without rounding each
- *    dequantised weight to BF16 (tf_dequant and tf_gemm keep that rounding).
+ *    slabs, each warp streams a contiguous run of them.  The codes enter the
+ *    tensor cores exactly (as FP16), x is converted to FP16 with a
+ *    power-of-two scale per 128-column block (exact), and (q - z) * s is
+ *    applied per group in FP32 to the sums: the result is
+ *    sum_k x * (q - z) * s without rounding each dequantised weight to BF16
+ *    (tf_dequant and tf_gemm keep that rounding).
  *  - The others (groups of 32, or x too large for the above) with K >= 1024
  *    and x resident: whole slabs per block (one block per slab on small
  *    layers), K split over the block's warps, each weight dequantised to
@@ -239,8 +240,8 @@ int tf_gemv_bias(const void* blob, size_t blob_bytes, int N, int K, int bits, in
 
 /*
  * Workspace bytes tf_gemm needs on the current device for this layer and M.
- * M <= 8 (K % 8 == 0): what the slab or tile GEMV behind it needs, as
- * tf_gemv_workspace_size (0 on layers with a 16-row slab per SM).  Else, to
+ * M <= 8 (K % 8 == 0): what the slab or tile GEMV behind it needs (0 for
+ * the slab GEMV: K >= 1024 with x resident in shared memory).  Else, to
  * split the K dimension of its last, partial wave of output tiles across
  * all SMs (stream-K): 16384 bytes of per-tile arrival counters, then FP32
  * partial sums, 0 when the tiles fill whole waves; plus, when K % 8 != 0
