@@ -13,9 +13,11 @@ one stream, bracketed by CUDA events with a device synchronisation on both
 sides; the GEMV step rotates through weight copies totalling more than 3x
 the L2 size so that every launch streams its weights from HBM.  Next to the
 headline the same run reports the square 8192 x 8192 layers (W8 per channel
-and W4 g64 at M = 1, 8, 64) and the large W4 g128 layers at M = 1, each as
-us per launch, GB/s and fraction of the measured HBM copy bandwidth, and
-the float64 oracle on all host cores (a process pool over output rows).
+and W4 g64 at M = 1, 8, 64), the large W4 g128 layers at M = 1 and 4096, and
+layers with fewer 16-row slabs than SMs, each as us per launch, GB/s,
+TFLOP/s and the fraction of the measured peak that bounds it (HBM copy
+bandwidth, or BF16 tensor throughput at M = 4096), and the float64 oracle on
+all host cores (a process pool over output rows).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -720,7 +722,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the square and large layer measurements")
+    ap.add_argument("--no-extras", action="store_true", help="skip the square, large and small-layer measurements")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
                     help="run one workload's launches a few times, untimed (for ncu captures)")
     ap.add_argument("--profile-reps", type=int, default=2)
